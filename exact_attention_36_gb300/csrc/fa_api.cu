@@ -1,0 +1,356 @@
+// fa_api.cu -- the extern "C" boundary of libfa_gb300.so (declared in
+// include/fa.h): argument checks, TMA tensor-map encoding, per-device set-up
+// and kernel launches.  The exp2 test kernels live here too.
+//
+// The library allocates no device memory.  Per-device state is limited to
+// cached attributes (SM count, compute capability) and the address of a
+// file-scope __device__ error word that bounded device waits write to.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "exp2_poly.cuh"
+#include "fa_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device error word (one per device that loads the library).
+__device__ int g_fa_error_word;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int *err_word = nullptr;  // device address of g_fa_error_word
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+thread_local int t_last_cuda_error = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+fa_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return FA_ERR_CUDA;
+}
+
+// Query (once per device) what the launches need.
+fa_status device_info(const DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        void *p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_fa_error_word)) != cudaSuccess) return cuda_fail(e);
+        d.err_word = static_cast<int *>(p);
+        d.ready = true;
+    }
+    // the kernels are built for sm_103a only
+    if (d.cc_major != 10 || d.cc_minor != 3) return FA_ERR_UNSUPPORTED;
+    *out = &d;
+    return FA_OK;
+}
+
+fa_status get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode ? FA_OK : FA_ERR_CUDA;
+}
+
+// Tensor map over a bf16 [B,S,H,D] tensor: dims (D, H, S, B), box
+// 64 x 1 x 128 x 1 (a 128-row x 128-byte tile), 128-byte swizzle, zero fill
+// outside the tensor (ragged sequence tails read as zeros).
+fa_status make_map_bshd(CUtensorMap *m, const void *ptr, int B, int S, int H, int D) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                                   (cuuint64_t)S * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared size/scale checks.  Sizes: B,H,S >= 1; D in the supported set;
+// one tensor below 2^31 elements.
+fa_status check_shape(int B, int H, int S, int D, float scale) {
+    if (B < 1 || H < 1 || S < 1) return FA_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const long long n = static_cast<long long>(B) * S * H * D;
+    if (D < 1 || n >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kDefaultRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 between rescales
+constexpr int kDefaultPolyGroups = 1;             // 1 of 8 column groups on the FMA exp2
+
+}  // namespace
+
+// ----------------------------------------------------------------- exp2 test kernels
+
+namespace {
+
+__device__ __forceinline__ float exp2_variant(float x, int variant) {
+    if (variant == 0) return fa::exp2_poly<3>(x);
+    if (variant == 1) return fa::exp2_poly_full<3>(x);
+    return fa::ex2_mufu(x);
+}
+
+__global__ void exp2_eval_kernel(const float *x, float *y, long long n, int variant) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        y[i] = exp2_variant(x[i], variant);
+}
+
+// Order-preserving map float bits <-> unsigned key (-inf < ... < -0 < +0 < ... ).
+__host__ __device__ __forceinline__ uint32_t float_key(uint32_t bits) {
+    return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t key_float(uint32_t key) {
+    return (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+}
+
+__global__ void exp2_sweep_init(unsigned long long *acc) { *acc = 0ull; }
+
+// Relative error |y - 2^x| / max(2^x, 2^-126), maximised over all floats
+// whose keys lie in [k_lo, k_lo + count).  The running maximum is kept as
+// (error as float bits) << 32 | (x bits), which orders by error.
+__global__ void exp2_sweep_kernel(uint32_t k_lo, unsigned long long count, int variant,
+                                  unsigned long long *acc) {
+    unsigned long long best = 0ull;
+    for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
+         i < count; i += (unsigned long long)gridDim.x * blockDim.x) {
+        const uint32_t bits = key_float(k_lo + static_cast<uint32_t>(i));
+        const float x = __uint_as_float(bits);
+        const float y = exp2_variant(x, variant);
+        const double ref = exp2(static_cast<double>(x));
+        const double den = fmax(ref, 1.1754943508222875e-38);  // 2^-126
+        const float err = static_cast<float>(fabs(static_cast<double>(y) - ref) / den);
+        const unsigned long long key =
+            (static_cast<unsigned long long>(__float_as_uint(err)) << 32) | bits;
+        best = key > best ? key : best;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+    }
+    if ((threadIdx.x & 31) == 0) atomicMax(acc, best);
+}
+
+__global__ void exp2_sweep_finish(double *out) {
+    const unsigned long long v = *reinterpret_cast<unsigned long long *>(out);
+    out[0] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(v >> 32)));
+    out[1] = static_cast<double>(__uint_as_float(static_cast<uint32_t>(v & 0xffffffffu)));
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- C ABI
+
+extern "C" {
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_last_cuda_error(int *cuda_err) {
+    if (!cuda_err) return FA_ERR_INVALID_ARG;
+    *cuda_err = t_last_cuda_error;
+    return FA_OK;
+}
+
+fa_status fa_device_error(int *code, int clear) {
+    if (!code) return FA_ERR_INVALID_ARG;
+    const DeviceInfo *d = nullptr;
+    fa_status st = device_info(&d);
+    if (st != FA_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    int v = 0;
+    if ((e = cudaMemcpy(&v, d->err_word, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e);
+    if (clear && v != 0) {
+        const int zero = 0;
+        if ((e = cudaMemcpy(d->err_word, &zero, sizeof(int), cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+    }
+    *code = v;
+    return v ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int H, int S, int D, int causal, float scale, float rescale_threshold,
+                    int poly_exp2_groups, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, S, D, scale);
+    if (st != FA_OK) return st;
+    if (rescale_threshold < 0.f) rescale_threshold = kDefaultRescaleThreshold;
+    if (!(rescale_threshold <= 16.f)) return FA_ERR_INVALID_ARG;
+    if (poly_exp2_groups < 0) poly_exp2_groups = kDefaultPolyGroups;
+    if (poly_exp2_groups != 0 && poly_exp2_groups != 1 && poly_exp2_groups != 2 &&
+        poly_exp2_groups != 8)
+        return FA_ERR_INVALID_ARG;
+    if (D == 256) return FA_ERR_UNSUPPORTED;
+    const DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != FA_OK) return st;
+    if ((st = get_encoder()) != FA_OK) return st;
+    fa::FwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.S = S;
+    a.D = D;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * kLog2e;
+    a.rescale_threshold = rescale_threshold;
+    a.poly_groups = poly_exp2_groups;
+    a.err_word = d->err_word;
+    a.num_sms = d->num_sms;
+    cudaError_t e = fa::launch_fwd(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int S, int D, int causal, float scale, void *stream) {
+    return fa_fwd_ex(q, k, v, o, lse, B, H, S, D, causal, scale, -1.f, -1, stream);
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t fa_bwd_workspace_size(int B, int H, int S, int D) {
+    if (check_shape(B, H, S, D, 1.f) != FA_OK) return 0;
+    const size_t n = static_cast<size_t>(B) * H * S;
+    return round256(n * D * sizeof(float)) + round256(n * sizeof(float));
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
+                 int B, int H, int S, int D, int causal, float scale, void *stream) {
+    const void *ptrs[11] = {q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, S, D, scale);
+    if (st != FA_OK) return st;
+    const DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != FA_OK) return st;
+    if ((st = get_encoder()) != FA_OK) return st;
+    fa::BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_do, dout, B, S, H, D)) != FA_OK) return st;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq_acc = dq_acc;
+    a.delta = delta;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.S = S;
+    a.D = D;
+    a.causal = causal ? 1 : 0;
+    a.scale = scale;
+    a.scale_log2 = scale * kLog2e;
+    a.err_word = d->err_word;
+    a.num_sms = d->num_sms;
+    cudaError_t e = fa::launch_bwd(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream) {
+    if (!x || !y || n < 0 || variant < 0 || variant > 2) return FA_ERR_INVALID_ARG;
+    if (n == 0) return FA_OK;
+    const DeviceInfo *d = nullptr;
+    fa_status st = device_info(&d);
+    if (st != FA_OK) return st;
+    const long long want = (n + 255) / 256;
+    const int grid = static_cast<int>(want < 8LL * d->num_sms ? want : 8LL * d->num_sms);
+    exp2_eval_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n, variant);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+fa_status fa_exp2_sweep(float lo, float hi, int variant, double *out, void *stream) {
+    if (!out || !(std::isfinite(lo) && std::isfinite(hi)) || lo > hi || variant < 0 ||
+        variant > 2)
+        return FA_ERR_INVALID_ARG;
+    const DeviceInfo *d = nullptr;
+    fa_status st = device_info(&d);
+    if (st != FA_OK) return st;
+    uint32_t blo, bhi;
+    std::memcpy(&blo, &lo, 4);
+    std::memcpy(&bhi, &hi, 4);
+    const uint32_t klo = float_key(blo), khi = float_key(bhi);
+    const unsigned long long count = static_cast<unsigned long long>(khi - klo) + 1ull;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto *acc = reinterpret_cast<unsigned long long *>(out);
+    exp2_sweep_init<<<1, 1, 0, s>>>(acc);
+    exp2_sweep_kernel<<<d->num_sms * 8, 256, 0, s>>>(klo, count, variant, acc);
+    exp2_sweep_finish<<<1, 1, 0, s>>>(out);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// fa_common.cuh -- launch-side declarations shared by the kernels' translation
+// units and the C-ABI layer (fa_api.cu).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Error codes written to the device error word by bounded waits that ran out.
+// The low byte names the wait site.
+enum DeviceError : int {
+    kErrNone = 0,
+    kErrFwdWait = 0x100,  // + site
+    kErrBwdWait = 0x200,  // + site
+};
+
+struct FwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v;  // bf16 [B,S,H,D], box 64 x 1 x 128 x 1, 128B swizzle
+    void *o;                       // bf16 [B,S,H,D]
+    float *lse;                    // fp32 [B,H,S]
+    int B, H, S, D;
+    int causal;
+    float scale_log2;         // softmax scale * log2(e)
+    float rescale_threshold;  // log2 units
+    int poly_groups;          // 16-column groups (of 8) that use the FMA exp2
+    int *err_word;            // device error word
+    int num_sms;
+};
+
+struct BwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [B,S,H,D], same boxes as the forward
+    const void *o, *dout;                 // bf16 [B,S,H,D]
+    const float *lse;                     // fp32 [B,H,S]
+    float *dq_acc;                        // fp32 [B,H,S,D]
+    float *delta;                         // fp32 [B,H,S]
+    void *dq, *dk, *dv;                   // bf16 [B,S,H,D]
+    int B, H, S, D;
+    int causal;
+    float scale;
+    float scale_log2;
+    int *err_word;
+    int num_sms;
+};
+
+// Launchers (defined in fa_fwd.cu / fa_bwd.cu).  Return the CUDA error of the
+// launch (cudaSuccess when enqueued).
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream);
+
+}  // namespace fa

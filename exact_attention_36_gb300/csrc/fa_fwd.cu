@@ -1,0 +1,485 @@
+// fa_fwd.cu -- fused attention forward for sm_103a (tcgen05 + TMA).
+//
+// Computes O = softmax(scale * Q K^T [+ causal mask]) V and the per-row
+// log-sum-exp, exactly (hyper.ai story on FlashAttention-4: faster without
+// changing the mathematical result).
+//
+// Design, after "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design
+// for Asymmetric Hardware Scaling" (gist.science/nl), Technische samenvatting:
+//   Methodologie §1  S = Q K^T and O += P V are asynchronous tcgen05 MMAs
+//                    whose accumulators live in Tensor Memory; 128x128 tiles;
+//                    the softmax of one query tile runs while the tensor core
+//                    works on the other ("ping-pong").
+//   Methodologie §2  2^x is split between MUFU.EX2 and an FMA polynomial.
+// and "FlashAttention-4: Der neue Rennwagen ..." (gist.science/de) §3: the
+// rescale of O is skipped unless the running maximum grew past a threshold.
+// Causal work is visited longest-first (hyper.ai story: LPT scheduling).
+//
+// CTA layout (320 threads, one CTA per SM, persistent over work units):
+//   warp 0       TMA producer: Q tile pair, then K_j / V_j into a ring of
+//                shared-memory slots guarded by full/empty mbarriers.
+//   warp 1       TMEM allocator and MMA issuer (one elected lane).
+//   warps 2-5    softmax + epilogue of query tile 0.
+//   warps 6-9    softmax + epilogue of query tile 1.
+// A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each group of four
+// consecutive warps covers the 128 lanes (= query rows) of its tile.
+// A work unit is (batch b, head h, 256 query rows = two 128-row tiles).
+//
+// Tensor Memory (512 columns x 128 lanes x 32 bit):
+//   [0,128)      S of tile 0; P (bf16 pairs) overwrites its first 64 columns
+//   [128,256)    S / P of tile 1
+//   [256,256+D)  O of tile 0;  [256+D, 256+2D) O of tile 1
+// The MMA warp issues, per key tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1).
+// tcgen05.mma instructions from one thread execute in issue order, so S(j+1)
+// overwrites the P(j) it aliases only after PV(j) has read it, and the
+// commit that signals S(j+1) also covers PV(j) (so the softmax may rescale O).
+#include "fa_common.cuh"
+#include "sm100_ptx.cuh"
+#include "exp2_poly.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kBlockM = 128;  // query rows per tile
+constexpr int kBlockN = 128;  // keys per tile
+constexpr int kBox = 16384;   // one TMA box: 128 rows x 64 bf16 (128 B), 128B swizzle
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kBoxes = D / 64;                // TMA boxes per 128-row tile
+    static constexpr int kTileBytes = kBox * kBoxes;     // 128 x D bf16
+    static constexpr int kStages = (D == 64) ? 8 : 4;    // ring slots (one K or V tile each)
+    static constexpr int kQBytes = 2 * kTileBytes;
+    static constexpr int kRingOff = kQBytes;
+    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 7;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+};
+
+struct Unit {
+    int bh;  // b * H + h
+    int p;   // query rows [256p, 256p + 256); -1: no unit for this CTA this round
+};
+
+// Work-unit order.  Units are numbered longest-first (p descending, which is
+// the order of decreasing work under a causal mask) with the head index
+// fastest; CTAs take them in a serpentine round-robin, which balances the
+// triangular causal work like an LPT list schedule.  Returns false when the
+// CTA has no further rounds.
+__device__ __forceinline__ bool unit_at(int it, int U, int BH, int P, Unit &out) {
+    const int G = gridDim.x;
+    const int base = it * G;
+    if (base >= U) return false;
+    const int c = (it & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int u = base + c;
+    if (u >= U) {
+        out.p = -1;
+        return true;
+    }
+    out.bh = u % BH;
+    out.p = P - 1 - u / BH;
+    return true;
+}
+
+// S = Q K^T for one 128x128 tile: both operands K-major (head dim contiguous).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_saddr, uint32_t k_saddr) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
+        mma_ss(tS, sdesc_sw128(q_saddr + off, 16, 1024), sdesc_sw128(k_saddr + off, 16, 1024),
+               FwdCfg<D>::kIdescS, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O (+)= P V: P from TMEM, V MN-major (head dim contiguous, keys along K).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_saddr, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        mma_ts(tO, tP + kk * 8, sdesc_sw128(v_saddr + kk * 2048, kBox, 1024),
+               FwdCfg<D>::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int D, int POLY_GROUPS>
+__global__ void __maxnreg__(200) fa_fwd_kernel(const __grid_constant__ FwdArgs args) {
+    using Cfg = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
+    uint64_t *q_full = bars + 0;
+    uint64_t *q_empty = bars + 1;
+    uint64_t *kv_full = bars + 2;
+    uint64_t *kv_empty = bars + 2 + Cfg::kStages;
+    uint64_t *s_full = bars + 2 + 2 * Cfg::kStages;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_full = s_full + 4;
+    uint64_t *drain = s_full + 6;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = args.H, S = args.S;
+    const int BH = args.B * H;
+    const int P = (S + 2 * kBlockM - 1) / (2 * kBlockM);
+    const int U = BH * P;
+    const int nKV = (S + kBlockN - 1) / kBlockN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < Cfg::kStages; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_full[t], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&args.tm_q);
+        tma_prefetch_desc(&args.tm_k);
+        tma_prefetch_desc(&args.tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t smem_base = smem_u32(smem);
+
+    // key tiles visited by query tile 0 / 1 of unit p
+    auto tiles_for = [&](int p, int &n0, int &n1) {
+        if (args.causal) {
+            n0 = min(2 * p * kBlockM + kBlockM - 1, S - 1) / kBlockN + 1;
+            n1 = min(2 * p * kBlockM + 2 * kBlockM - 1, S - 1) / kBlockN + 1;
+        } else {
+            n0 = n1 = nKV;
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 1};
+            uint32_t ring = 0, qi = 0;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                Unit un;
+                if (!unit_at(it, U, BH, P, un)) break;
+                if (un.p < 0) continue;
+                const int b = un.bh / H, h = un.bh % H;
+                int n0, n1;
+                tiles_for(un.p, n0, n1);
+                w.code = kErrFwdWait + 1;
+                if (!mbar_wait(q_empty, (qi & 1) ^ 1, w)) { ok = false; break; }
+                ++qi;
+                mbar_arrive_expect_tx(q_full, Cfg::kQBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_4d(smem + t * Cfg::kTileBytes + c * kBox, &args.tm_q, q_full,
+                                    64 * c, h, 2 * un.p * kBlockM + t * kBlockM, b);
+                for (int j = 0; j < n1 && ok; ++j) {
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t slot = ring % Cfg::kStages;
+                        w.code = kErrFwdWait + 2;
+                        if (!mbar_wait(&kv_empty[slot], ((ring / Cfg::kStages) & 1) ^ 1, w)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&kv_full[slot], Cfg::kTileBytes);
+                        uint8_t *dst = smem + Cfg::kRingOff + slot * Cfg::kTileBytes;
+                        const CUtensorMap *map = which ? &args.tm_v : &args.tm_k;
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_load_4d(dst + c * kBox, map, &kv_full[slot], 64 * c, h,
+                                        j * kBlockN, b);
+                        ++ring;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                const uint32_t lo = ring > (uint32_t)Cfg::kStages ? ring - Cfg::kStages : 0;
+                for (uint32_t r = lo; r < ring; ++r)
+                    mbar_wait_drain(&kv_full[r % Cfg::kStages], (r / Cfg::kStages) & 1);
+                if (qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 10};
+            uint32_t ring = 0, qi = 0;
+            uint32_t pph0 = 0, pph1 = 0;
+            const uint32_t tS0 = tmem, tS1 = tmem + 128;
+            const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
+            const uint32_t q0 = smem_base, q1 = smem_base + Cfg::kTileBytes;
+            const uint32_t ring_base = smem_base + Cfg::kRingOff;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                Unit un;
+                if (!unit_at(it, U, BH, P, un)) break;
+                if (un.p < 0) continue;
+                int n0, n1;
+                tiles_for(un.p, n0, n1);
+                w.code = kErrFwdWait + 10;
+                if (!mbar_wait(q_full, qi & 1, w)) { ok = false; break; }
+                ++qi;
+                const uint32_t kslot = ring % Cfg::kStages;
+                w.code = kErrFwdWait + 11;
+                if (!mbar_wait(&kv_full[kslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                ++ring;
+                tc_fence_after();
+                issue_qk<D>(tS0, q0, ring_base + kslot * Cfg::kTileBytes);
+                mma_commit(&s_full[0]);
+                issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
+                mma_commit(&s_full[1]);
+                mma_commit(&kv_empty[kslot]);
+                for (int j = 0; j < n1; ++j) {
+                    const uint32_t vslot = ring % Cfg::kStages;
+                    w.code = kErrFwdWait + 12;
+                    if (!mbar_wait(&kv_full[vslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                    ++ring;
+                    const bool has_next = (j + 1 < n1);
+                    uint32_t nslot = 0, nphase = 0;
+                    if (has_next) {
+                        nslot = ring % Cfg::kStages;
+                        nphase = (ring / Cfg::kStages) & 1;
+                        ++ring;
+                    }
+                    const uint32_t vaddr = ring_base + vslot * Cfg::kTileBytes;
+                    const uint32_t naddr = ring_base + nslot * Cfg::kTileBytes;
+                    bool next_ready = false;
+                    if (j < n0) {
+                        w.code = kErrFwdWait + 13;
+                        if (!mbar_wait(&p_full[0], pph0, w)) { ok = false; break; }
+                        pph0 ^= 1;
+                        tc_fence_after();
+                        issue_pv<D>(tO0, tS0, vaddr, j > 0);
+                        if (j + 1 < n0) {
+                            w.code = kErrFwdWait + 14;
+                            if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
+                            next_ready = true;
+                            tc_fence_after();
+                            issue_qk<D>(tS0, q0, naddr);
+                            mma_commit(&s_full[0]);
+                        } else {
+                            mma_commit(&o_full[0]);
+                        }
+                    }
+                    w.code = kErrFwdWait + 15;
+                    if (!mbar_wait(&p_full[1], pph1, w)) { ok = false; break; }
+                    pph1 ^= 1;
+                    tc_fence_after();
+                    issue_pv<D>(tO1, tS1, vaddr, j > 0);
+                    mma_commit(&kv_empty[vslot]);
+                    if (has_next) {
+                        if (!next_ready) {
+                            w.code = kErrFwdWait + 16;
+                            if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        issue_qk<D>(tS1, q1, naddr);
+                        mma_commit(&s_full[1]);
+                        mma_commit(&kv_empty[nslot]);
+                    } else {
+                        mma_commit(&o_full[1]);
+                        mma_commit(q_empty);
+                    }
+                }
+            }
+            // every MMA issued must have finished before TMEM is released
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = (warp - 2) >> 2;  // query tile of this warpgroup
+        const int quarter = warp & 3;   // TMEM lane quarter this warp may access
+        const int r_in_tile = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + t * 128 + lane_off;
+        const uint32_t tO = tmem + 256 + t * D + lane_off;
+        const float c2 = args.scale_log2;
+        const float tau = args.rescale_threshold;
+        WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 20 + t};
+        uint32_t sph = 0, oph = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            Unit un;
+            if (!unit_at(it, U, BH, P, un)) break;
+            if (un.p < 0) continue;
+            const int b = un.bh / H, h = un.bh % H;
+            int n0, n1;
+            tiles_for(un.p, n0, n1);
+            const int n = t ? n1 : n0;
+            const int row = 2 * un.p * kBlockM + t * kBlockM + r_in_tile;
+            float m_used = -INFINITY;  // reference maximum, log2 units of scaled scores
+            float l = 0.f;             // running row sum relative to m_used
+            for (int j = 0; j < n; ++j) {
+                if (!mbar_wait(&s_full[t], sph, w)) { ok = false; break; }
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                if (j == n - 1) {
+                    // last tile of the row: keys past S and, if causal, past the row
+                    const int lim = (args.causal ? min(row, S - 1) : S - 1) - j * kBlockN;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+                }
+                float mx[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    mx[c] = __uint_as_float(sr[c][0]);
+#pragma unroll
+                    for (int e = 1; e < 32; ++e) mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][e]));
+                }
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+                const float m_new = fmaxf(m_used, m_tile);
+                if (__any_sync(0xffffffffu, m_new > m_used + tau)) {
+                    // conditional rescale: move the reference maximum to m_new
+                    const float alpha = ex2_mufu(m_used - m_new);
+                    l *= alpha;
+                    if (j > 0) {
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t orr[32];
+                            tmem_ld32(tO + c * 32, orr);
+                            tmem_ld_wait(orr);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                            tmem_st32(tO + c * 32, orr);
+                        }
+                    }
+                    m_used = m_new;
+                }
+                const float neg_m = -m_used;
+                float lsum[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float x0 = fmaf(__uint_as_float(sr[c][e]), c2, neg_m);
+                        const float x1 = fmaf(__uint_as_float(sr[c][e + 1]), c2, neg_m);
+                        float p0, p1;
+                        if ((((c * 32 + e) >> 4) & 7) < POLY_GROUPS) {
+                            p0 = exp2_poly<3>(x0);
+                            p1 = exp2_poly<3>(x1);
+                        } else {
+                            p0 = ex2_mufu(x0);
+                            p1 = ex2_mufu(x1);
+                        }
+                        acc += p0 + p1;
+                        pk[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    lsum[c] = acc;
+                    // P columns [16c, 16c+16) hold keys [32c, 32c+32); they
+                    // overwrite S columns whose values are already in registers
+                    tmem_st16(tS + c * 16, pk);
+                }
+                l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&p_full[t]);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16, LSE
+            if (!mbar_wait(&o_full[t], oph, w)) { ok = false; break; }
+            oph ^= 1;
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            uint16_t *orow = reinterpret_cast<uint16_t *>(args.o) +
+                             ((static_cast<size_t>(b) * S + row) * H + h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(tO + c * 32, orr);
+                tmem_ld_wait(orr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                                        __uint_as_float(orr[2 * e + 1]) * inv_l);
+                if (row < S) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                             pk[4 * v4 + 3]);
+                }
+            }
+            if (row < S)
+                args.lse[(static_cast<size_t>(b) * H + h) * S + row] =
+                    (m_used + log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+template <int D, int PG>
+cudaError_t launch_fwd_inst(const FwdArgs &a, cudaStream_t stream) {
+    using Cfg = FwdCfg<D>;
+    auto kern = fa_fwd_kernel<D, PG>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long P = (a.S + 255) / 256;
+    const long long U = static_cast<long long>(a.B) * a.H * P;
+    const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
+    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream) {
+    switch (a.poly_groups) {
+        case 0: return launch_fwd_inst<D, 0>(a, stream);
+        case 1: return launch_fwd_inst<D, 1>(a, stream);
+        case 2: return launch_fwd_inst<D, 2>(a, stream);
+        case 8: return launch_fwd_inst<D, 8>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
+    switch (a.D) {
+        case 64: return launch_fwd_d<64>(a, stream);
+        case 128: return launch_fwd_d<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa

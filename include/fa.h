@@ -1,0 +1,153 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library libfa_gb300.so.
+ *
+ * Sources cited below:
+ *   [hyper] hyper.ai story on FlashAttention-4 (German): exact attention,
+ *           faster without changing the mathematical result; 128x128 tiles;
+ *           LPT scheduling for causal masks.
+ *   [nl]    "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+ *           Asymmetric Hardware Scaling" (gist.science/nl), section
+ *           "Technische samenvatting": Methodologie §1 (asynchronous MMA into
+ *           Tensor Memory, 128x128 tiles, ping-pong of softmax and MMA),
+ *           §2 (exp2 split between the MUFU unit and an FMA polynomial of
+ *           degree 3 or 5), §3 (backward pass: intermediates in Tensor Memory,
+ *           2-CTA MMA, dQ reduced by atomic additions in global memory).
+ *   [de]    "FlashAttention-4: Der neue Rennwagen fuer die kuenstliche
+ *           Intelligenz" (gist.science/de), §3: the rescale of the running
+ *           output is skipped unless it is really needed.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, contiguous, row-major.  Q, K, V, O, dO, dQ, dK, dV
+ *     are bf16 [B, S, H, D] (element (b,s,h,d) at ((b*S + s)*H + h)*D + d).
+ *     LSE and Delta are fp32 [B, H, S]; the dQ accumulator is fp32
+ *     [B, H, S, D].
+ *   - Every pointer is a device pointer, owned by the caller, 16-byte aligned.
+ *     The library allocates no device memory, keeps no state across calls
+ *     and never synchronises the device (except fa_device_error).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: results are ready when the stream reaches them.
+ *   - Supported: D in {64, 128, 256}; any S >= 1; B, H >= 1 with B*S*H*D
+ *     below 2^31 elements per tensor; scale finite and > 0.  causal != 0
+ *     means key j is visible to query i iff j <= i.
+ *   - Errors: FA_ERR_INVALID_ARG for a null or misaligned pointer, a
+ *     non-positive size, overflow or a bad scale; FA_ERR_UNSUPPORTED for a
+ *     head dim outside the supported set or a device without tcgen05
+ *     (compute capability 10.x); FA_ERR_CUDA when a CUDA call or launch
+ *     fails (see fa_last_cuda_error).  Nothing is enqueued when an error is
+ *     returned by the argument checks.
+ *   - Device-side waits are bounded.  A wait that runs out (which correct
+ *     code never reaches) records a code that fa_device_error reports; the
+ *     kernel then returns instead of hanging.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,
+    FA_ERR_UNSUPPORTED = 2,
+    FA_ERR_CUDA = 3,
+    FA_ERR_TIMEOUT = 4
+} fa_status;
+
+/*
+ * Forward: O = softmax(scale * Q K^T [+ causal mask]) V and
+ * LSE[b,h,i] = ln sum_{j visible} exp(scale * q_i . k_j)   ([hyper]; [nl]
+ * Methodologie §1).  One fused, persistent kernel: TMA loads into a
+ * multi-stage shared-memory ring, tcgen05 MMAs into Tensor Memory, two
+ * 128-row query tiles per CTA whose softmax ping-pongs with the tensor core,
+ * conditional rescale of O ([de] §3), exp2 split between MUFU and a degree-3
+ * polynomial ([nl] Methodologie §2), longest-first tile order for causal
+ * masks ([hyper]).
+ *   q, k, v : bf16 [B,S,H,D] inputs.      o   : bf16 [B,S,H,D] output.
+ *   lse     : fp32 [B,H,S] output (natural log of the scaled, masked scores).
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int H, int S, int D, int causal, float scale, void *stream);
+
+/*
+ * Forward with explicit numerics knobs (used to test that they do not change
+ * the result beyond rounding).
+ *   rescale_threshold : the running maximum (log2 units) may grow by this
+ *                       much before O and the row sum are rescaled; 0 means
+ *                       rescale whenever the maximum grows ([de] §3).
+ *                       Range [0, 16]; a negative value selects the default.
+ *   poly_exp2_groups  : how many of the eight 16-column groups of each
+ *                       128-wide score tile take exp2 from the FMA
+ *                       polynomial instead of MUFU ([nl] Methodologie §2):
+ *                       one of 0 (MUFU only), 1, 2, 8 (polynomial only);
+ *                       -1 selects the library default.
+ */
+fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int H, int S, int D, int causal, float scale,
+                    float rescale_threshold, int poly_exp2_groups, void *stream);
+
+/*
+ * Bytes of caller-provided scratch the backward pass needs: the fp32 dQ
+ * accumulator [B,H,S,D] followed by fp32 Delta [B,H,S], each rounded up to
+ * 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int S, int D);
+
+/*
+ * Backward ([nl] Methodologie §3): given Q, K, V, the forward output O, its
+ * LSE and the upstream gradient dO, computes
+ *   Delta_i = dO_i . O_i, dS = P o (dO V^T - Delta), dV = P^T dO,
+ *   dK = scale dS^T Q, dQ = scale dS K,   P = exp(scale Q K^T - LSE).
+ * Three launches on `stream`: Delta + zeroing of the dQ accumulator; the
+ * fused main kernel (K/V-stationary, intermediates in Tensor Memory, dQ by
+ * fp32 atomic additions); conversion of the accumulator to bf16 dQ.
+ *   dq_acc : fp32 [B,H,S,D] scratch (contents on entry ignored).
+ *   delta  : fp32 [B,H,S] scratch (written).
+ *   dq, dk, dv : bf16 [B,S,H,D] outputs.
+ * dq_acc/delta may be carved from one buffer of fa_bwd_workspace_size bytes.
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const void *dout, const float *lse, float *dq_acc, float *delta,
+                 void *dq, void *dk, void *dv,
+                 int B, int H, int S, int D, int causal, float scale, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *fa_status_string(fa_status s);
+
+/* The last cudaError_t seen by any entry point of this thread (0 if none);
+ * returns FA_OK. */
+fa_status fa_last_cuda_error(int *cuda_err);
+
+/*
+ * Synchronises the current device, then reports and (if clear != 0) resets
+ * the device-side error word that bounded waits set when they run out.
+ * *code = 0 means no wait ever ran out.  Returns FA_ERR_TIMEOUT when the
+ * word is non-zero, FA_ERR_CUDA if the synchronisation fails.
+ */
+fa_status fa_device_error(int *code, int clear);
+
+/*
+ * Test hooks for the exp2 approximation ([nl] Methodologie §2; degree 3,
+ * accurate enough because bf16 rounding dominates its error).
+ * fa_exp2_eval: y[i] = approximate 2^x[i] for n device floats.
+ *   variant 0 = the softmax kernel's polynomial (inputs below -125 are
+ *               clamped, giving a value in (0, 2^-124]),
+ *   variant 1 = the same polynomial with exact subnormal scaling,
+ *   variant 2 = hardware MUFU ex2.approx (flush-to-zero).
+ * fa_exp2_sweep: every fp32 x with lo <= x <= hi (lo, hi finite, lo <= hi)
+ *   is evaluated with `variant` and compared to 2^x in double precision;
+ *   the largest relative error |y - 2^x| / max(2^x, 2^-126) and its
+ *   argument are written to out[0], out[1] (device doubles; out[0] is also
+ *   used as an accumulator while the sweep runs).
+ */
+fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream);
+fa_status fa_exp2_sweep(float lo, float hi, int variant, double *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -15,14 +15,17 @@
 // rescale of O is skipped unless the running maximum grew past a threshold.
 // Causal work is visited longest-first (hyper.ai story: LPT scheduling).
 //
-// CTA layout (320 threads, one CTA per SM, persistent over work units):
+// CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent over
+// work units):
 //   warp 0       TMA producer: Q tile pair, then K_j / V_j into a ring of
 //                shared-memory slots guarded by full/empty mbarriers.
 //   warp 1       TMEM allocator and MMA issuer (one elected lane).
-//   warps 2-5    softmax + epilogue of query tile 0.
-//   warps 6-9    softmax + epilogue of query tile 1.
-// A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each group of four
-// consecutive warps covers the 128 lanes (= query rows) of its tile.
+//   warps 2-3    idle (they complete warpgroup 0).
+//   warps 4-7    softmax + epilogue of query tile 0.
+//   warps 8-11   softmax + epilogue of query tile 1.
+// A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each warpgroup
+// covers the 128 lanes (= query rows) of its tile.  Each SM sub-partition
+// holds three warps (one of each warpgroup), so a thread gets 168 registers.
 // A work unit is (batch b, head h, 256 query rows = two 128-row tiles).
 //
 // Tensor Memory (512 columns x 128 lanes x 32 bit):
@@ -40,7 +43,7 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per tile
 constexpr int kBox = 16384;   // one TMA box: 128 rows x 64 bf16 (128 B), 128B swizzle
@@ -109,7 +112,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_sa
 }
 
 template <int D, int POLY_GROUPS>
-__global__ void __maxnreg__(200) fa_fwd_kernel(const __grid_constant__ FwdArgs args) {
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs args) {
     using Cfg = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -309,9 +312,9 @@ __global__ void __maxnreg__(200) fa_fwd_kernel(const __grid_constant__ FwdArgs a
             mma_commit(drain);
             mbar_wait_drain(drain, 0);
         }
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax + epilogue
-        const int t = (warp - 2) >> 2;  // query tile of this warpgroup
+        const int t = (warp - 4) >> 2;  // query tile of this warpgroup
         const int quarter = warp & 3;   // TMEM lane quarter this warp may access
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;

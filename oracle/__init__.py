@@ -34,7 +34,7 @@ def _load():
         L, I, Dd = ctypes.c_long, ctypes.c_int, ctypes.c_double
         lib.fa_oracle_fwd.argtypes = [dp, dp, dp, L, L, I, Dd, lp, L, dp, dp]
         lib.fa_oracle_fwd.restype = I
-        lib.fa_oracle_bwd_stats.argtypes = [dp, dp, dp, dp, L, L, I, Dd, dp, dp, dp]
+        lib.fa_oracle_bwd_stats.argtypes = [dp, dp, dp, dp, L, L, I, Dd, lp, L, dp, dp, dp]
         lib.fa_oracle_bwd_stats.restype = I
         lib.fa_oracle_bwd_dq.argtypes = [dp, dp, dp, dp, dp, dp, L, L, I, Dd, lp, L, dp]
         lib.fa_oracle_bwd_dq.restype = I
@@ -119,7 +119,7 @@ def backward_head(q, k, v, dout, causal: bool, scale: float, rows=None, cols=Non
     delta = np.empty((S,), np.float64)
     o = np.empty((S, D), np.float64) if want_o else None
     rc = lib.fa_oracle_bwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), S, D, int(causal),
-                                 float(scale), _ptr(lse), _ptr(delta),
+                                 float(scale), None, S, _ptr(lse), _ptr(delta),
                                  _ptr(o) if o is not None else None)
     if rc != 0:
         raise MemoryError("oracle backward stats: allocation failed")
@@ -145,6 +145,40 @@ def backward_head(q, k, v, dout, causal: bool, scale: float, rows=None, cols=Non
     if want_o:
         out["o"] = o
     return out
+
+
+def row_stats_head(q, k, v, dout, causal: bool, scale: float, rows):
+    """LSE_i and Delta_i (= sum_j P_ij dP_ij) of one head for the listed rows.
+
+    Returns (lse [n], delta [n]) as an (n,)-array pair.
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    S, D = q.shape
+    rows_a, n = _idx(rows)
+    lse = np.empty((n,), np.float64)
+    delta = np.empty((n,), np.float64)
+    rc = _load().fa_oracle_bwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), S, D, int(causal),
+                                     float(scale), _lptr(rows_a), n, _ptr(lse), _ptr(delta), None)
+    if rc != 0:
+        raise MemoryError("oracle row stats: allocation failed")
+    return lse, delta
+
+
+def dq_rows_head(q, k, v, dout, lse_full, delta_full, causal: bool, scale: float, rows):
+    """Rows of dQ of one head given LSE/Delta arrays indexed by row (only the
+    listed rows' entries are read)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    S, D = q.shape
+    rows_a, n = _idx(rows)
+    lse_full = np.ascontiguousarray(lse_full, dtype=np.float64)
+    delta_full = np.ascontiguousarray(delta_full, dtype=np.float64)
+    dq = np.empty((n, D), np.float64)
+    rc = _load().fa_oracle_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse_full),
+                                  _ptr(delta_full), S, D, int(causal), float(scale),
+                                  _lptr(rows_a), n, _ptr(dq))
+    if rc != 0:
+        raise MemoryError("oracle dq: allocation failed")
+    return dq
 
 
 def forward(q, k, v, causal: bool, scale: float, heads=None, rows=None):

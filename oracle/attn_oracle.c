@@ -129,14 +129,16 @@ int fa_oracle_fwd(const double *q, const double *k, const double *v, long S, lon
 }
 
 /*
- * Row statistics for the backward pass, for every row i of the head:
- *   lse[i]   = LSE_i (as in the forward),
- *   delta[i] = Delta_i = sum_j P_ij dP_ij with dP_ij = dO_i . V_j,
- *   o (optional, may be NULL) = O, the exact forward output.
+ * Row statistics for the backward pass, for the listed rows (rows == NULL:
+ * every row i of the head, in order):
+ *   lse[r]   = LSE_i (as in the forward),
+ *   delta[r] = Delta_i = sum_j P_ij dP_ij with dP_ij = dO_i . V_j,
+ *   o (optional, may be NULL) row r = O_i, the exact forward output.
  */
 int fa_oracle_bwd_stats(const double *q, const double *k, const double *v,
                         const double *dout, long S, long D, int causal, double scale,
-                        double *lse, double *delta, double *o) {
+                        const long *rows, long nrows, double *lse, double *delta, double *o) {
+    if (rows == NULL) nrows = S;
     double *kt = transpose(k, S, D);
     double *vt = transpose(v, S, D);
     if (!kt || !vt) { free(kt); free(vt); return -1; }
@@ -151,17 +153,18 @@ int fa_oracle_bwd_stats(const double *q, const double *k, const double *v,
             fail = 1;
         } else {
 #pragma omp for schedule(dynamic, 4)
-            for (long i = 0; i < S; ++i) {
+            for (long r = 0; r < nrows; ++r) {
+                const long i = rows ? rows[r] : r;
                 const long n = n_visible(i, S, causal);
                 score_row(q + i * D, kt, S, D, n, scale, s);
-                lse[i] = softmax_row(s, n, p);
+                lse[r] = softmax_row(s, n, p);
                 /* dP_ij = dO_i . V_j (no scale: dP is the gradient w.r.t. P) */
                 score_row(dout + i * D, vt, S, D, n, 1.0, dp);
                 double acc = 0.0;
                 for (long j = 0; j < n; ++j) acc += p[j] * dp[j];
-                delta[i] = acc;
+                delta[r] = acc;
                 if (o) {
-                    double *oi = o + i * D;
+                    double *oi = o + r * D;
                     for (long d = 0; d < D; ++d) oi[d] = 0.0;
                     for (long j = 0; j < n; ++j)
                         for (long d = 0; d < D; ++d) oi[d] += p[j] * v[j * D + d];

@@ -259,3 +259,18 @@ def test_input_recipe_is_seeded_and_stress_scales_one_percent_of_keys():
         top = norms[0, :, h].topk(3).values
         assert (top > 8).all()
     assert qs.float().abs().max() > 8  # Q ~ N(0, 4^2)
+
+
+def test_row_stats_and_dq_rows_match_full_backward():
+    S, D = 40, 8
+    q, k, v, do = _rand_head(S, D, 50)
+    full = oracle.backward_head(q, k, v, do, True, 0.4)
+    rows = [39, 2, 17]
+    lse, delta = oracle.row_stats_head(q, k, v, do, True, 0.4, rows)
+    np.testing.assert_array_equal(lse, full["lse"][rows])
+    np.testing.assert_array_equal(delta, full["delta"][rows])
+    lf = np.zeros(S); df = np.zeros(S)
+    lf[rows] = lse
+    df[rows] = delta
+    dq = oracle.dq_rows_head(q, k, v, do, lf, df, True, 0.4, rows)
+    np.testing.assert_array_equal(dq, full["dq"][rows])

@@ -1,7 +1,635 @@
-// fa_bwd.cu -- fused attention backward for sm_103a (placeholder launcher
-// until the backward kernels land).
+// fa_bwd.cu -- fused attention backward for sm_103a (tcgen05 + TMA).
+//
+// Given Q, K, V, O, dO and LSE, computes dQ, dK, dV of exact softmax
+// attention ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+// Asymmetric Hardware Scaling" (gist.science/nl), Technische samenvatting,
+// Methodologie §3: the backward pass keeps its intermediates in Tensor Memory
+// because shared-memory bandwidth is its bottleneck; dQ is reduced with
+// atomic additions in global memory).  With P = exp(scale*S - LSE):
+//   Delta_i = dO_i . O_i,   dS = P o (dO V^T - Delta),
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
+//
+// Three launches:
+//   fa_bwd_prep     Delta = rowsum(dO o O) (fp32) and dQ accumulator = 0
+//   fa_bwd_kernel   the fused main kernel (below)
+//   fa_bwd_dq_cvt   dQ = bf16(scale * accumulator)
+//
+// Main kernel: persistent, one CTA per SM, a work unit is (b, h, key tile j
+// of 128 keys).  K_j and V_j stay in shared memory; 128-query blocks Q_i,
+// dO_i stream through.  Everything is computed transposed (keys on the 128
+// TMEM lanes), so P^T and dS^T land in Tensor Memory exactly where the dV
+// and dK MMAs want their A operand:
+//   S^T  = K_j Q_i^T      -> X   (fp32, 128 cols)    A=K smem, B=Q smem
+//   dP^T = V_j dO_i^T     -> Y   (fp32, 128 cols)    A=V smem, B=dO smem
+//   P^T (bf16) over X;  dS^T (bf16) over Y and into shared memory
+//   dV  += P^T dO_i       (TMEM acc, D cols)         A=X tmem,  B=dO smem
+//   dK  += dS^T Q_i       (TMEM acc, D cols)         A=Y tmem,  B=Q smem
+//   dQ_i = dS K_j  -> Y   (fp32, queries on lanes)   A=dS smem, B=K smem
+// Tensor Memory: X [0,128) | Y [128,256) | dV [256,256+D) | dK [256+D,256+2D).
+// tcgen05.mma from one thread executes in issue order: S(i+1) may overwrite
+// X once dV(i) was issued, dQ(i) may overwrite Y once dK(i) was issued.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer (K_j/V_j per unit; Q_i + LSE/Delta, dO_i per block)
+//   warp 1      TMEM allocation + MMA issue (one lane)
+//   warps 2-3   idle
+//   warps 4-7   "softmax": P^T and dS^T for one 128x128 block (lane = key)
+//   warps 8-11  dQ drain (lane = query, fp32 atomic add into the accumulator)
+//               and the dK / dV epilogue of each unit
+// Causal units are visited longest first (key tile 0 sees every query
+// block) in a serpentine order over the CTAs, as in the forward.
+#include <cuda_bf16.h>
+
 #include "fa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kBlk = 128;    // keys per unit and queries per block
+constexpr int kBox = 16384;  // one TMA box: 128 rows x 64 bf16, 128B swizzle
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kTile = kBox * kBoxes;  // 128 x D bf16
+    // shared memory map
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTile;
+    static constexpr int kOffQ = kOffV + kTile;      // 2 stages
+    static constexpr int kOffDO = kOffQ + 2 * kTile;  // 1 stage
+    static constexpr int kOffDS = kOffDO + kTile;     // dS: 128 keys x 128 queries bf16
+    static constexpr int kOffStat = kOffDS + 32768;   // 2 stages x (128 lse2 + 128 delta) fp32
+    static constexpr int kOffBar = kOffStat + 2 * 1024;
+    // kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full,
+    // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dkdv_empty, drain
+    static constexpr int kNumBars = 17;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTX = 0, kTY = 128, kTdV = 256, kTdK = 256 + D;
+    static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+    static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);    // dV, dK
+    static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, true, true);      // dQ
+};
+
+struct BUnit {
+    int bh;  // b * H + h
+    int j;   // key tile; -1 = no unit for this CTA this round
+};
+
+__device__ __forceinline__ bool bunit_at(int it, int U, int BH, BUnit &out) {
+    const int G = gridDim.x;
+    const int base = it * G;
+    if (base >= U) return false;
+    const int c = (it & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int u = base + c;
+    if (u >= U) {
+        out.j = -1;
+        return true;
+    }
+    out.bh = u % BH;
+    out.j = u / BH;  // key tile 0 first: under a causal mask it has the most blocks
+    return true;
+}
+
+// first query block a key tile sees (causal: queries >= first key)
+__device__ __forceinline__ int first_block(int j, int causal) { return causal ? j : 0; }
+
+// ---------------------------------------------------------------- MMA helpers
+
+// 128x128 (x D) with both operands K-major: S^T = K Q^T, dP^T = V dO^T
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t tD, uint32_t a_saddr, uint32_t b_saddr) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
+        mma_ss(tD, sdesc_sw128(a_saddr + off, 16, 1024), sdesc_sw128(b_saddr + off, 16, 1024),
+               BwdCfg<D>::kIdescSS, kk > 0 ? 1u : 0u);
+    }
+}
+
+// acc (+)= A[tmem: 128 keys x 128 queries] * B[smem: 128 queries x D, MN-major]
+template <int D>
+__device__ __forceinline__ void issue_acc(uint32_t tAcc, uint32_t tA, uint32_t b_saddr, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < kBlk / 16; ++kk)
+        mma_ts(tAcc, tA + kk * 8, sdesc_sw128(b_saddr + kk * 2048, kBox, 1024),
+               BwdCfg<D>::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+}
+
+// dQ = dS K: A = dS (queries x keys, MN-major: rows = keys), B = K (keys x D, MN-major)
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t tD, uint32_t ds_saddr, uint32_t k_saddr) {
+#pragma unroll
+    for (int kk = 0; kk < kBlk / 16; ++kk)
+        mma_ss(tD, sdesc_sw128(ds_saddr + kk * 2048, kBox, 1024),
+               sdesc_sw128(k_saddr + kk * 2048, kBox, 1024), BwdCfg<D>::kIdescDQ,
+               kk > 0 ? 1u : 0u);
+}
+
+
+// ---------------------------------------------------------------- main kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdArgs args) {
+    using Cfg = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1;
+    uint64_t *q_full = bars + 2, *q_empty = bars + 4;  // [2] each
+    uint64_t *do_full = bars + 6, *do_empty = bars + 7;
+    uint64_t *s_full = bars + 8, *dp_full = bars + 9;
+    uint64_t *p_ready = bars + 10, *ds_ready = bars + 11;
+    uint64_t *dq_full = bars + 12, *dq_empty = bars + 13;
+    uint64_t *dkdv_full = bars + 14, *dkdv_empty = bars + 15;
+    uint64_t *drain = bars + 16;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
+    float *stat = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // [stage][lse2 128 | delta 128]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = args.H, S = args.S;
+    const int BH = args.B * H;
+    const int nT = (S + kBlk - 1) / kBlk;  // key tiles = query blocks
+    const int U = BH * nT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s2 = 0; s2 < 2; ++s2) {
+            mbar_init(&q_full[s2], 1);
+            mbar_init(&q_empty[s2], 1);
+        }
+        mbar_init(do_full, 1);
+        mbar_init(do_empty, 1);
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_ready, 128);
+        mbar_init(ds_ready, 128);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 128);
+        mbar_init(dkdv_full, 1);
+        mbar_init(dkdv_empty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&args.tm_q);
+        tma_prefetch_desc(&args.tm_k);
+        tma_prefetch_desc(&args.tm_v);
+        tma_prefetch_desc(&args.tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t sbase = smem_u32(smem);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 1};
+        uint32_t nunit = 0, nblk = 0;  // units / blocks issued so far
+        bool ok = true;
+        const float log2e = 1.4426950408889634f;
+        for (int it = 0; ok; ++it) {
+            BUnit un;
+            if (!bunit_at(it, U, BH, un)) break;
+            if (un.j < 0) continue;
+            const int b = un.bh / H, h = un.bh % H;
+            const int i0 = first_block(un.j, args.causal);
+            if (lane == 0) {
+                w.code = kErrBwdWait + 1;
+                ok = mbar_wait(kv_empty, (nunit & 1) ^ 1, w);
+                if (ok) {
+                    mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
+                    for (int c = 0; c < Cfg::kBoxes; ++c) {
+                        tma_load_4d(smem + Cfg::kOffK + c * kBox, &args.tm_k, kv_full, 64 * c, h,
+                                    un.j * kBlk, b);
+                        tma_load_4d(smem + Cfg::kOffV + c * kBox, &args.tm_v, kv_full, 64 * c, h,
+                                    un.j * kBlk, b);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            ++nunit;
+            for (int i = i0; i < nT && ok; ++i, ++nblk) {
+                const int st = nblk & 1;
+                // Q_i (+ LSE and Delta of its rows) into stage st
+                w.code = kErrBwdWait + 2;
+                ok = mbar_wait(&q_empty[st], ((nblk >> 1) & 1) ^ 1, w);
+                ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
+                if (!ok) break;
+                float *sl = stat + st * 256;
+                const size_t rbase = static_cast<size_t>(un.bh) * S;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int qr = r * 32 + lane;
+                    const int q = i * kBlk + qr;
+                    const bool in = q < S;
+                    sl[qr] = in ? args.lse[rbase + q] * log2e : INFINITY;
+                    sl[128 + qr] = in ? args.delta[rbase + q] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_4d(smem + Cfg::kOffQ + st * Cfg::kTile + c * kBox, &args.tm_q,
+                                    &q_full[st], 64 * c, h, i * kBlk, b);
+                    // dO_i (single stage)
+                    w.code = kErrBwdWait + 3;
+                    ok = mbar_wait(do_empty, (nblk & 1) ^ 1, w);
+                    if (ok) {
+                        mbar_arrive_expect_tx(do_full, Cfg::kTile);
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_load_4d(smem + Cfg::kOffDO + c * kBox, &args.tm_do, do_full,
+                                        64 * c, h, i * kBlk, b);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            }
+        }
+        if (!ok && lane == 0) {
+            // let issued copies land before the CTA exits
+            if (nunit > 0) mbar_wait_drain(kv_full, (nunit - 1) & 1);
+            if (nblk > 0) {
+                mbar_wait_drain(&q_full[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1);
+                mbar_wait_drain(do_full, (nblk - 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 10};
+            const uint32_t tX = tmem + Cfg::kTX, tY = tmem + Cfg::kTY;
+            const uint32_t tdV = tmem + Cfg::kTdV, tdK = tmem + Cfg::kTdK;
+            const uint32_t aK = sbase + Cfg::kOffK, aV = sbase + Cfg::kOffV;
+            const uint32_t aDO = sbase + Cfg::kOffDO, aDS = sbase + Cfg::kOffDS;
+            uint32_t nunit = 0, nblk = 0;
+            uint32_t ph_p = 0, ph_ds = 0, ph_dqe = 0;
+            bool ok = true;
+#define FA_WAIT(bar, par, site)                                  \
+    do {                                                         \
+        w.code = kErrBwdWait + (site);                           \
+        if (!mbar_wait((bar), (par), w)) { ok = false; break; } \
+    } while (0)
+            for (int it = 0; ok; ++it) {
+                BUnit un;
+                if (!bunit_at(it, U, BH, un)) break;
+                if (un.j < 0) continue;
+                const int i0 = first_block(un.j, args.causal);
+                FA_WAIT(kv_full, nunit & 1, 10);
+                if (!ok) break;
+                // first block: S^T and dP^T (the previous unit's last dQ was
+                // drained before its dP would have been issued; wait for it here)
+                {
+                    const int st = nblk & 1;
+                    FA_WAIT(&q_full[st], (nblk >> 1) & 1, 11);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_kmajor<D>(tX, aK, sbase + Cfg::kOffQ + st * Cfg::kTile);
+                    mma_commit(s_full);
+                    if (nblk > 0) {
+                        FA_WAIT(dq_empty, ph_dqe, 12);
+                        if (!ok) break;
+                        ph_dqe ^= 1;
+                    }
+                    FA_WAIT(do_full, nblk & 1, 13);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_kmajor<D>(tY, aV, aDO);
+                    mma_commit(dp_full);
+                }
+                for (int i = i0; i < nT; ++i, ++nblk) {
+                    const int st = nblk & 1;
+                    const bool first = (i == i0), has_next = (i + 1 < nT);
+                    FA_WAIT(p_ready, ph_p, 14);
+                    if (!ok) break;
+                    ph_p ^= 1;
+                    if (first && nunit > 0) {
+                        // previous unit's dK/dV epilogue has read the accumulators
+                        FA_WAIT(dkdv_empty, (nunit - 1) & 1, 15);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    issue_acc<D>(tdV, tX, aDO, !first);
+                    mma_commit(do_empty);
+                    if (has_next) {
+                        const int st2 = (nblk + 1) & 1;
+                        FA_WAIT(&q_full[st2], ((nblk + 1) >> 1) & 1, 16);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_kmajor<D>(tX, aK, sbase + Cfg::kOffQ + st2 * Cfg::kTile);
+                        mma_commit(s_full);
+                    }
+                    FA_WAIT(ds_ready, ph_ds, 17);
+                    if (!ok) break;
+                    ph_ds ^= 1;
+                    tc_fence_after();
+                    issue_acc<D>(tdK, tY, sbase + Cfg::kOffQ + st * Cfg::kTile, !first);
+                    mma_commit(&q_empty[st]);
+                    issue_dq<D>(tY, aDS, aK);
+                    mma_commit(dq_full);
+                    if (has_next) {
+                        FA_WAIT(dq_empty, ph_dqe, 18);
+                        if (!ok) break;
+                        ph_dqe ^= 1;
+                        FA_WAIT(do_full, (nblk + 1) & 1, 19);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_kmajor<D>(tY, aV, aDO);
+                        mma_commit(dp_full);
+                    } else {
+                        mma_commit(dkdv_full);
+                        mma_commit(kv_empty);
+                    }
+                }
+                ++nunit;
+            }
+#undef FA_WAIT
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    }
+    else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P^T and dS^T
+        const int quarter = warp & 3;
+        const int kr = quarter * 32 + lane;  // key row of the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tX = tmem + Cfg::kTX + lane_off, tY = tmem + Cfg::kTY + lane_off;
+        const float c2 = args.scale_log2;
+        WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 30};
+        uint32_t n = 0;
+        bool ok = true;
+        uint8_t *ds_row = smem + Cfg::kOffDS + kr * 128;
+        const int sw = kr & 7;  // 128B swizzle phase of this row
+        for (int it = 0; ok; ++it) {
+            BUnit un;
+            if (!bunit_at(it, U, BH, un)) break;
+            if (un.j < 0) continue;
+            const int i0 = first_block(un.j, args.causal);
+            const int key = un.j * kBlk + kr;
+            for (int i = i0; i < nT; ++i, ++n) {
+                const int st = n & 1;
+                w.code = kErrBwdWait + 30;
+                if (!mbar_wait(&q_full[st], (n >> 1) & 1, w)) { ok = false; break; }
+                w.code = kErrBwdWait + 31;
+                if (!mbar_wait(s_full, n & 1, w)) { ok = false; break; }
+                tc_fence_after();
+                const float *lse2 = stat + st * 256;
+                const float *dlt = lse2 + 128;
+                uint32_t pk[64];
+                {
+                    uint32_t sr[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tX + c * 32, sr[c]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                    // visible: key < S and (non-causal or query >= key); rows
+                    // past S carry lse2 = +inf, which gives P = 0
+                    const bool key_ok = key < S;
+                    const bool diag = args.causal && (i == un.j);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c * 32 + e);
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            float p[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int col = c * 32 + e + u;
+                                const bool vis = key_ok && !(diag && col < kr);
+                                p[u] = vis ? ex2_mufu(fmaf(__uint_as_float(sr[c][e + u]), c2, -lv[u]))
+                                           : 0.f;
+                            }
+                            pk[(c * 32 + e) / 2] = pack_bf16x2(p[0], p[1]);
+                            pk[(c * 32 + e) / 2 + 1] = pack_bf16x2(p[2], p[3]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_st16(tX + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_ready);
+                // ---- dS^T = P^T o (dP^T - Delta)
+                w.code = kErrBwdWait + 32;
+                if (!mbar_wait(dp_full, n & 1, w)) { ok = false; break; }
+                if (n > 0) {
+                    // the dQ MMA of the previous block has finished reading dS
+                    w.code = kErrBwdWait + 33;
+                    if (!mbar_wait(dq_full, (n - 1) & 1, w)) { ok = false; break; }
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t dr[32];
+                    tmem_ld32(tY + c * 32, dr);
+                    tmem_ld_wait(dr);
+                    uint32_t dsw[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4 *>(dlt + c * 32 + e);
+                        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float ds[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t pw = pk[(c * 32 + e + u) >> 1];
+                            const float pv = __uint_as_float(((e + u) & 1) ? (pw & 0xffff0000u) : (pw << 16));
+                            ds[u] = pv * (__uint_as_float(dr[e + u]) - dv4[u]);
+                        }
+                        dsw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                        dsw[e / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+                    }
+                    tmem_st16(tY + c * 16, dsw);
+                    // shared copy for the dQ MMA: queries [32c, 32c+32) of this key row,
+                    // 128B-swizzled, two 64-query blocks of 16 KB
+                    uint8_t *blk = ds_row + (c >> 1) * kBox;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int chunk = (c & 1) * 4 + t;
+                        *reinterpret_cast<uint4 *>(blk + ((chunk ^ sw) << 4)) =
+                            make_uint4(dsw[4 * t], dsw[4 * t + 1], dsw[4 * t + 2], dsw[4 * t + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(ds_ready);
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // TMEM lane: query (dQ) or key (dK, dV)
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 40};
+        uint32_t n = 0, nunit = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            BUnit un;
+            if (!bunit_at(it, U, BH, un)) break;
+            if (un.j < 0) continue;
+            const int b = un.bh / H, h = un.bh % H;
+            const int i0 = first_block(un.j, args.causal);
+            for (int i = i0; i < nT; ++i, ++n) {
+                w.code = kErrBwdWait + 40;
+                if (!mbar_wait(dq_full, n & 1, w)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t acc[D];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    tmem_ld32(tmem + Cfg::kTY + lane_off + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&acc[c * 32]));
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&acc[c * 32]));
+                tc_fence_before();
+                mbar_arrive(dq_empty);
+                const int q = i * kBlk + r;
+                if (q < S) {
+                    float *dst = args.dq_acc + (static_cast<size_t>(un.bh) * S + q) * D;
+#pragma unroll
+                    for (int d = 0; d < D; d += 4)
+                        red_add_v4(dst + d, __uint_as_float(acc[d]), __uint_as_float(acc[d + 1]),
+                                   __uint_as_float(acc[d + 2]), __uint_as_float(acc[d + 3]));
+                }
+            }
+            if (!ok) break;
+            w.code = kErrBwdWait + 41;
+            if (!mbar_wait(dkdv_full, nunit & 1, w)) { ok = false; break; }
+            ++nunit;
+            tc_fence_after();
+            const int key = un.j * kBlk + r;
+            const size_t orow = ((static_cast<size_t>(b) * S + key) * H + h) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
+                const float mul = which ? args.scale : 1.f;
+                uint16_t *out = reinterpret_cast<uint16_t *>(which ? args.dk : args.dv) + orow;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tsrc + c * 32, v);
+                    tmem_ld_wait(v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
+                                            __uint_as_float(v[2 * e + 1]) * mul);
+                    if (key < S) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                 pk[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(dkdv_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+// ---------------------------------------------------------------- prep / convert
+
+// One warp per (b, h, query row): Delta = sum_d dO * O (fp32), and the row of
+// the dQ accumulator set to zero.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdArgs args) {
+    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long rows = static_cast<long long>(args.B) * args.H * args.S;
+    if (row >= rows) return;
+    const int S = args.S, H = args.H;
+    const int q = static_cast<int>(row % S);
+    const long long bh = row / S;
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    const size_t off = ((static_cast<size_t>(b) * S + q) * H + h) * D;
+    constexpr int kPer = D / 32;  // bf16 per lane
+    const __nv_bfloat16 *po = reinterpret_cast<const __nv_bfloat16 *>(args.o) + off + lane * kPer;
+    const __nv_bfloat16 *pd = reinterpret_cast<const __nv_bfloat16 *>(args.dout) + off + lane * kPer;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+        const float2 o2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(po + e));
+        const float2 d2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pd + e));
+        acc = fmaf(o2.x, d2.x, acc);
+        acc = fmaf(o2.y, d2.y, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) args.delta[row] = acc;
+    float4 *z = reinterpret_cast<float4 *>(args.dq_acc + static_cast<size_t>(row) * D);
+#pragma unroll
+    for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One warp per (b, h, query row): dQ[b, q, h, :] = bf16(scale * accumulator).
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_dq_cvt(const __grid_constant__ BwdArgs args) {
+    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long rows = static_cast<long long>(args.B) * args.H * args.S;
+    if (row >= rows) return;
+    const int S = args.S, H = args.H;
+    const int q = static_cast<int>(row % S);
+    const long long bh = row / S;
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    const float *src = args.dq_acc + static_cast<size_t>(row) * D;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(args.dq) +
+                                                 ((static_cast<size_t>(b) * S + q) * H + h) * D);
+#pragma unroll
+    for (int e = lane; e < D / 2; e += 32) {
+        const float2 a = reinterpret_cast<const float2 *>(src)[e];
+        dst[e] = pack_bf16x2(a.x * args.scale, a.y * args.scale);
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
+    using Cfg = BwdCfg<D>;
+    const long long rows = static_cast<long long>(a.B) * a.H * a.S;
+    const long long blocks = (rows * 32 + 255) / 256;
+    fa_bwd_prep<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = fa_bwd_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
+    const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
+    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
+    switch (a.D) {
+        case 64: return launch_bwd_d<64>(a, stream);
+        case 128: return launch_bwd_d<128>(a, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 }  // namespace fa

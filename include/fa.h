@@ -114,6 +114,27 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  void *dq, void *dk, void *dv,
                  int B, int H, int S, int D, int causal, float scale, void *stream);
 
+/*
+ * Backward for callers that cannot allocate device memory: code that runs
+ * where cudaMalloc is not allowed or not wanted (host callbacks, plug-ins
+ * that only get their inputs and outputs from a host framework, tools that
+ * must keep the device footprint fixed).  The pages have no counterpart of
+ * this entry point; it exists for those callers only.
+ * Same arguments, results and errors as fa_bwd minus dq_acc and delta
+ * (sizes that fa_bwd_workspace_size rejects give FA_ERR_INVALID_ARG); the
+ * scratch comes from one fixed array of 72 MiB inside the library, held on
+ * every GPU that loads the library until the process exits.  Problems whose
+ * scratch (fa_bwd_workspace_size) exceeds 72 MiB are rejected with
+ * FA_ERR_INVALID_ARG.  The first call on each device looks up the array's
+ * device address (make it before any stream capture).  All calls on a
+ * device share the array: calls whose kernels may overlap on the GPU race
+ * and must be serialised by the caller.  Each call re-zeroes the part of the
+ * scratch it uses, so nothing carries over between calls.  Allocates nothing.
+ */
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                         int B, int H, int S, int D, int causal, float scale, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *fa_status_string(fa_status s);
 

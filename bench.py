@@ -302,6 +302,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for quick runs)")
+    ap.add_argument("--seq", type=int, default=WORKLOAD["S"],
+                    help="sequence length override (profiling runs on a smaller case)")
+    ap.add_argument("--only-noncausal", action="store_true",
+                    help="skip the causal measurement and the e2e loop (profiling runs)")
     return ap.parse_args()
 
 
@@ -365,7 +369,10 @@ def main():
     from exact_attention_36_gb300.inputs import make_qkvdo
 
     fa_build.build()
-    W = WORKLOAD
+    W = dict(WORKLOAD)
+    if args.seq != W["S"]:
+        W["S"] = args.seq
+        W["name"] = f"B1_H16_S{args.seq}_D128"
     B, H, S, D = W["B"], W["H"], W["S"], W["D"]
     scale = 1.0 / math.sqrt(D)
     # every rank draws its own batch (weak scaling over independent heads)
@@ -377,9 +384,14 @@ def main():
     with ClockSampler(local_rank) as clk:
         ms, fwd_ms, bwd_ms = time_device(buf, False, scale, args.steps, args.warmup, dist_on)
     clocks = clk.summary()
-    ms_c, fwd_ms_c, bwd_ms_c = time_device(buf, True, scale, args.steps, args.warmup, dist_on)
-    e2e_ms, h2d, d2h = time_e2e(q, k, v, do, buf, False, scale, args.steps, args.warmup,
-                                dist_on)
+    if args.only_noncausal:
+        ms_c = fwd_ms_c = bwd_ms_c = float("nan")
+        e2e_ms, h2d, d2h = float("nan"), 0, 0
+    else:
+        ms_c, fwd_ms_c, bwd_ms_c = time_device(buf, True, scale, args.steps, args.warmup,
+                                               dist_on)
+        e2e_ms, h2d, d2h = time_e2e(q, k, v, do, buf, False, scale, args.steps, args.warmup,
+                                    dist_on)
     assert fa.device_error() == 0, "a bounded device wait ran out"
 
     ff, fb = flops(B, H, S, D, False)
@@ -415,9 +427,12 @@ def main():
                      "frac": achieved / peak, "traffic": traffic},
         "e2e": {"value": world * (ff + fb) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 4 * args.steps,  # fa_fwd 1 + fa_bwd 3 per step of the value's region
         "clocks": clocks,
     }
+    if args.only_noncausal:
+        line["causal"] = None
+        line["e2e"] = None
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_sample(q, k, v, do, False, scale)
     if rank == 0:

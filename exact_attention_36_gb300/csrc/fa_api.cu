@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/fa.h"
+#include "fa.h"
 #include "exp2_poly.cuh"
 #include "fa_common.cuh"
 #include "sm100_ptx.cuh"

@@ -19,7 +19,7 @@
 // rewrites Delta, so nothing is carried over from an earlier call.
 #include <mutex>
 
-#include "../../include/fa.h"
+#include "fa.h"
 
 namespace {
 

@@ -107,6 +107,24 @@ fa_status make_map_bshd(CUtensorMap *m, const void *ptr, int B, int S, int H, in
     return FA_OK;
 }
 
+// Tensor map over the fp32 dQ accumulator viewed as [B*H][S][D]: box
+// 32 x 128 x 1 (128 rows x 128 bytes), 128-byte swizzle; rows past S are
+// outside the tensor, so reductions into them are dropped.
+fa_status make_map_dqacc(CUtensorMap *m, void *ptr, int BH, int S, int D) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)S * D * 4};
+    const cuuint32_t box[3] = {32, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shared size/scale checks.  Sizes: B,H,S >= 1; D in the supported set;
@@ -296,6 +314,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_do, dout, B, S, H, D)) != FA_OK) return st;
+    if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, B * H, S, D)) != FA_OK) return st;
     a.o = o;
     a.dout = dout;
     a.lse = lse;

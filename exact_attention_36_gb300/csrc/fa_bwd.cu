@@ -60,13 +60,16 @@ struct BwdCfg {
     static constexpr int kOffQ = kOffV + kTile;      // 2 stages
     static constexpr int kOffDO = kOffQ + 2 * kTile;  // 1 stage
     static constexpr int kOffDS = kOffDO + kTile;     // dS: 128 keys x 128 queries bf16
-    static constexpr int kOffStat = kOffDS + 32768;   // 2 stages x (128 lse2 + 128 delta) fp32
+    static constexpr int kOffRed = kOffDS + 32768;    // dQ staging: 2 x (128 rows x 32 fp32)
+    static constexpr int kOffStat = kOffRed + 32768;  // 2 stages x (128 lse2 + 128 delta) fp32
     static constexpr int kOffBar = kOffStat + 2 * 1024;
     // kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full,
     // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dkdv_empty, drain
     static constexpr int kNumBars = 17;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    // no alignment slack: the dynamic shared memory base must be 1024-byte
+    // aligned (checked at kernel entry)
+    static constexpr int kSmemBytes = kOffMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTX = 0, kTY = 128, kTdV = 256, kTdK = 256 + D;
     static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
@@ -135,9 +138,12 @@ __device__ __forceinline__ void issue_dq(uint32_t tD, uint32_t ds_saddr, uint32_
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdArgs args) {
     using Cfg = BwdCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicCAS(args.err_word, 0, kErrBwdWait + 0xff);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint64_t *kv_full = bars + 0, *kv_empty = bars + 1;
     uint64_t *q_full = bars + 2, *q_empty = bars + 4;  // [2] each
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
         for (int s2 = 0; s2 < 2; ++s2) {
-            mbar_init(&q_full[s2], 1);
+            mbar_init(&q_full[s2], 2);  // TMA (expect_tx) + LSE/Delta written
             mbar_init(&q_empty[s2], 1);
         }
         mbar_init(do_full, 1);
@@ -188,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         tma_prefetch_desc(&args.tm_k);
         tma_prefetch_desc(&args.tm_v);
         tma_prefetch_desc(&args.tm_do);
+        tma_prefetch_desc(&args.tm_dqacc);
     }
     tc_fence_before();
     __syncthreads();
@@ -229,6 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 ok = mbar_wait(&q_empty[st], ((nblk >> 1) & 1) ^ 1, w);
                 ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
                 if (!ok) break;
+                if (lane == 0) {
+                    // the tile first, so its latency overlaps the LSE/Delta loads
+                    mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_4d(smem + Cfg::kOffQ + st * Cfg::kTile + c * kBox, &args.tm_q,
+                                    &q_full[st], 64 * c, h, i * kBlk, b);
+                }
                 float *sl = stat + st * 256;
                 const size_t rbase = static_cast<size_t>(un.bh) * S;
 #pragma unroll
@@ -241,10 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
-                    for (int c = 0; c < Cfg::kBoxes; ++c)
-                        tma_load_4d(smem + Cfg::kOffQ + st * Cfg::kTile + c * kBox, &args.tm_q,
-                                    &q_full[st], 64 * c, h, i * kBlk, b);
+                    mbar_arrive(&q_full[st]);
                     // dO_i (single stage)
                     w.code = kErrBwdWait + 3;
                     ok = mbar_wait(do_empty, (nblk & 1) ^ 1, w);
@@ -396,24 +407,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
                     // visible: key < S and (non-causal or query >= key); rows
                     // past S carry lse2 = +inf, which gives P = 0
-                    const bool key_ok = key < S;
-                    const bool diag = args.causal && (i == un.j);
+                    // masking only where a block can hold invisible pairs: the
+                    // causal diagonal block and a key tile reaching past S
+                    // (queries past S carry lse2 = +inf, which gives P = 0)
+                    if ((args.causal && i == un.j) || (un.j + 1) * kBlk > S) {
+                        const int lim = (args.causal && i == un.j) ? kr : -1;  // col < lim hidden
+                        const bool key_ok = key < S;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (!key_ok || c * 32 + e < lim)
+                                    sr[c][e] = __float_as_uint(-INFINITY);
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4) {
                             const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c * 32 + e);
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                            float p[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int col = c * 32 + e + u;
-                                const bool vis = key_ok && !(diag && col < kr);
-                                p[u] = vis ? ex2_mufu(fmaf(__uint_as_float(sr[c][e + u]), c2, -lv[u]))
-                                           : 0.f;
-                            }
-                            pk[(c * 32 + e) / 2] = pack_bf16x2(p[0], p[1]);
-                            pk[(c * 32 + e) / 2 + 1] = pack_bf16x2(p[2], p[3]);
+                            const float p0 = ex2_mufu(fmaf(__uint_as_float(sr[c][e]), c2, -l4.x));
+                            const float p1 = ex2_mufu(fmaf(__uint_as_float(sr[c][e + 1]), c2, -l4.y));
+                            const float p2 = ex2_mufu(fmaf(__uint_as_float(sr[c][e + 2]), c2, -l4.z));
+                            const float p3 = ex2_mufu(fmaf(__uint_as_float(sr[c][e + 3]), c2, -l4.w));
+                            pk[(c * 32 + e) / 2] = pack_bf16x2(p0, p1);
+                            pk[(c * 32 + e) / 2 + 1] = pack_bf16x2(p2, p3);
                         }
                     }
                 }
@@ -433,10 +450,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t dr[32];
-                    tmem_ld32(tY + c * 32, dr);
-                    tmem_ld_wait(dr);
+                for (int c2i = 0; c2i < 4; c2i += 2) {
+                  uint32_t drr[2][32];
+                  tmem_ld32(tY + c2i * 32, drr[0]);
+                  tmem_ld32(tY + c2i * 32 + 32, drr[1]);
+                  tmem_ld_wait(drr[0]);
+                  tmem_ld_wait(drr[1]);
+#pragma unroll
+                  for (int c = c2i; c < c2i + 2; ++c) {
+                    const uint32_t (&dr)[32] = drr[c - c2i];
                     uint32_t dsw[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
@@ -462,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         *reinterpret_cast<uint4 *>(blk + ((chunk ^ sw) << 4)) =
                             make_uint4(dsw[4 * t], dsw[4 * t + 1], dsw[4 * t + 2], dsw[4 * t + 3]);
                     }
+                  }
                 }
                 fence_proxy_async_smem();
                 tmem_st_wait();
@@ -471,11 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        // dQ_i is staged 32 columns at a time in 128B-swizzled shared memory
+        // and added into the fp32 accumulator by TMA bulk reductions, which
+        // keeps the atomics off the load/store pipe the softmax warps use.
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // TMEM lane: query (dQ) or key (dK, dV)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const bool leader = (threadIdx.x == 256);
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 40};
-        uint32_t n = 0, nunit = 0;
+        uint32_t n = 0, nunit = 0, nred = 0;
         bool ok = true;
         for (int it = 0; ok; ++it) {
             BUnit un;
@@ -497,13 +524,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&acc[c * 32]));
                 tc_fence_before();
                 mbar_arrive(dq_empty);
-                const int q = i * kBlk + r;
-                if (q < S) {
-                    float *dst = args.dq_acc + (static_cast<size_t>(un.bh) * S + q) * D;
 #pragma unroll
-                    for (int d = 0; d < D; d += 4)
-                        red_add_v4(dst + d, __uint_as_float(acc[d]), __uint_as_float(acc[d + 1]),
-                                   __uint_as_float(acc[d + 2]), __uint_as_float(acc[d + 3]));
+                for (int c = 0; c < D / 32; ++c, ++nred) {
+                    uint8_t *buf = smem + Cfg::kOffRed + (nred & 1) * 16384;
+                    if (leader) bulk_wait_read<1>();  // the reduction that last used buf has read it
+                    named_bar_sync(1, 128);
+                    uint8_t *row = buf + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4 *>(row + ((k ^ (r & 7)) << 4)) =
+                            make_uint4(acc[c * 32 + 4 * k], acc[c * 32 + 4 * k + 1],
+                                       acc[c * 32 + 4 * k + 2], acc[c * 32 + 4 * k + 3]);
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
+                    if (leader) {
+                        tma_reduce_add_3d(&args.tm_dqacc, buf, 32 * c, i * kBlk, un.bh);
+                        bulk_commit();
+                    }
                 }
             }
             if (!ok) break;
@@ -540,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             tc_fence_before();
             mbar_arrive(dkdv_empty);
         }
+        if (leader) bulk_wait<0>();
     }
 
     tc_fence_before();

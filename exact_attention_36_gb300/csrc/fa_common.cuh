@@ -30,6 +30,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [B,S,H,D], same boxes as the forward
+    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 128 x 1, 128B swizzle
     const void *o, *dout;                 // bf16 [B,S,H,D]
     const float *lse;                     // fp32 [B,H,S]
     float *dq_acc;                        // fp32 [B,H,S,D]

@@ -13,6 +13,7 @@
 // coefficients are a relative-error minimax fit made by fit_exp2_poly.py.
 #pragma once
 #include "exp2_poly_coeffs.h"
+#include "sm100_ptx.cuh"
 
 namespace fa {
 
@@ -60,6 +61,23 @@ __device__ __forceinline__ float exp2_poly_full(float x) {
     const float p = exp2_poly_core<DEG>(f);
     const float big = __int_as_float(__float_as_int(p) + ((__float_as_int(t) + 64) << 23));
     return __fmul_rn(big, 5.42101086242752217e-20f);  // * 2^-64
+}
+
+// Two lanes at once, the kernel variant's arithmetic with two-lane fp32
+// instructions (same rounding, same results as exp2_poly<3> per lane).
+__device__ __forceinline__ float2 exp2_poly3_x2(float2 x) {
+    const float2 kShift = make_float2(12582912.0f, 12582912.0f);
+    x.x = fmaxf(x.x, -125.0f);
+    x.y = fmaxf(x.y, -125.0f);
+    const float2 t = add2(x, kShift);
+    const float2 n = add2(t, make_float2(-12582912.0f, -12582912.0f));
+    const float2 f = fma2(n, make_float2(-1.0f, -1.0f), x);
+    float2 p = fma2(make_float2(FA_EXP2_P3_C3, FA_EXP2_P3_C3), f,
+                    make_float2(FA_EXP2_P3_C2, FA_EXP2_P3_C2));
+    p = fma2(p, f, make_float2(FA_EXP2_P3_C1, FA_EXP2_P3_C1));
+    p = fma2(p, f, make_float2(FA_EXP2_P3_C0, FA_EXP2_P3_C0));
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
 }
 
 }  // namespace fa

@@ -23,7 +23,7 @@ struct FwdArgs {
     int causal;
     float scale_log2;         // softmax scale * log2(e)
     float rescale_threshold;  // log2 units
-    int poly_groups;          // 16-column groups (of 8) that use the FMA exp2
+    int poly_groups;          // columns of every 8 whose exp2 uses the FMA polynomial
     int *err_word;            // device error word
     int num_sms;
 };

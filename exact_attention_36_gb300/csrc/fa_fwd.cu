@@ -111,7 +111,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_sa
     }
 }
 
-template <int D, int POLY_GROUPS>
+template <int D, int POLY_PER8>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs args) {
     using Cfg = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -354,14 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
                 }
+                // row maximum: four independent chains of 3-input max
                 float mx[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    mx[c] = __uint_as_float(sr[c][0]);
+                    mx[c] = fmax3(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]),
+                                  __uint_as_float(sr[c][2]));
 #pragma unroll
-                    for (int e = 1; e < 32; ++e) mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][e]));
+                    for (int e = 3; e < 31; e += 2)
+                        mx[c] = fmax3(mx[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                    mx[c] = fmaxf(mx[c], __uint_as_float(sr[c][31]));
                 }
-                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+                const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * c2;
                 const float m_new = fmaxf(m_used, m_tile);
                 if (__any_sync(0xffffffffu, m_new > m_used + tau)) {
                     // conditional rescale: move the reference maximum to m_new
@@ -381,33 +385,38 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     }
                     m_used = m_new;
                 }
-                const float neg_m = -m_used;
-                float lsum[4];
+                // p = 2^(s*c2 - m_used): in every group of 8 columns the last
+                // POLY_PER8 go to the FMA polynomial, the rest to MUFU, so both
+                // units work at once; arguments and row sums use two-lane fp32
+                const float2 c2v = make_float2(c2, c2);
+                const float2 nmv = make_float2(-m_used, -m_used);
+                float2 lsum[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
-                    float acc = 0.f;
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float x0 = fmaf(__uint_as_float(sr[c][e]), c2, neg_m);
-                        const float x1 = fmaf(__uint_as_float(sr[c][e + 1]), c2, neg_m);
-                        float p0, p1;
-                        if ((((c * 32 + e) >> 4) & 7) < POLY_GROUPS) {
-                            p0 = exp2_poly<3>(x0);
-                            p1 = exp2_poly<3>(x1);
+                        const float2 xv = fma2(make_float2(__uint_as_float(sr[c][e]),
+                                                           __uint_as_float(sr[c][e + 1])),
+                                               c2v, nmv);
+                        float2 pv;
+                        if ((e & 7) >= 8 - POLY_PER8) {
+                            pv = exp2_poly3_x2(xv);
                         } else {
-                            p0 = ex2_mufu(x0);
-                            p1 = ex2_mufu(x1);
+                            pv.x = ex2_mufu(xv.x);
+                            pv.y = ex2_mufu(xv.y);
                         }
-                        acc += p0 + p1;
-                        pk[e >> 1] = pack_bf16x2(p0, p1);
+                        acc = add2(acc, pv);
+                        pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
                     }
                     lsum[c] = acc;
                     // P columns [16c, 16c+16) hold keys [32c, 32c+32); they
                     // overwrite S columns whose values are already in registers
                     tmem_st16(tS + c * 16, pk);
                 }
-                l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+                const float2 ls = add2(add2(lsum[0], lsum[1]), add2(lsum[2], lsum[3]));
+                l += ls.x + ls.y;
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[t]);

@@ -79,11 +79,11 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *                       much before O and the row sum are rescaled; 0 means
  *                       rescale whenever the maximum grows ([de] §3).
  *                       Range [0, 16]; a negative value selects the default.
- *   poly_exp2_groups  : how many of the eight 16-column groups of each
- *                       128-wide score tile take exp2 from the FMA
- *                       polynomial instead of MUFU ([nl] Methodologie §2):
- *                       one of 0 (MUFU only), 1, 2, 8 (polynomial only);
- *                       -1 selects the library default.
+ *   poly_exp2_groups  : how many of every 8 consecutive score columns take
+ *                       exp2 from the FMA polynomial instead of MUFU ([nl]
+ *                       Methodologie §2): one of 0 (MUFU only), 1 (12.5 %),
+ *                       2 (25 %), 8 (polynomial only); -1 selects the
+ *                       library default.
  */
 fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                     int B, int H, int S, int D, int causal, float scale,
@@ -157,7 +157,9 @@ fa_status fa_device_error(int *code, int clear);
  *   variant 0 = the softmax kernel's polynomial (inputs below -125 are
  *               clamped, giving a value in (0, 2^-124]),
  *   variant 1 = the same polynomial with exact subnormal scaling,
- *   variant 2 = hardware MUFU ex2.approx (flush-to-zero).
+ *   variant 2 = hardware MUFU ex2.approx (flush-to-zero),
+ *   variant 3 = the kernel polynomial in its two-lane (f32x2) form, as the
+ *               softmax evaluates it (same range and clamp as variant 0).
  * fa_exp2_sweep: every fp32 x with lo <= x <= hi (lo, hi finite, lo <= hi)
  *   is evaluated with `variant` and compared to 2^x in double precision;
  *   the largest relative error |y - 2^x| / max(2^x, 2^-126) and its

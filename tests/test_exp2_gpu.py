@@ -31,6 +31,16 @@ def test_kernel_polynomial_exhaustive_on_its_range():
     assert err <= 1e-4  # the degree-3 fit itself is ~7.5e-5
 
 
+def test_two_lane_polynomial_matches_scalar_kernel_polynomial():
+    # the softmax evaluates the polynomial with f32x2 instructions; same
+    # rounding per lane, so the two forms agree bit for bit
+    g = torch.Generator().manual_seed(9)
+    x = (-140.0 + 160.0 * torch.rand(1 << 20, generator=g)).cuda()
+    assert torch.equal(fa.exp2_eval(x, 3), fa.exp2_eval(x, 0))
+    err, xm = fa.exp2_sweep(-125.0, 16.0, variant=3)
+    assert err <= GATE, (err, xm)
+
+
 def test_kernel_polynomial_clamps_below_minus125():
     x = torch.tensor([-125.5, -126.0, -127.0, -150.0, -1e30, float("-inf")], device="cuda")
     y = fa.exp2_eval(x, variant=0).cpu().double()

@@ -151,11 +151,15 @@ def cpu_sample(q, k, v, dout, causal, scale, target_s=12.0):
     import oracle
 
     S = q.shape[1]
-    probe = pick_rows(S, 32, seed=1)
-    dt0, _ = oracle_sample(q, k, v, dout, causal, scale, probe)
-    n = int(max(32, min(S, 32 * target_s / max(dt0, 1e-3))))
-    rows = pick_rows(S, n, seed=2)
-    dt, fl = oracle_sample(q, k, v, dout, causal, scale, rows)
+    n = 32
+    dt, fl = oracle_sample(q, k, v, dout, causal, scale, pick_rows(S, n, seed=2))
+    # grow the sample until it is about target_s of CPU work (fixed per-call
+    # costs make the first estimate low)
+    for _ in range(3):
+        if dt >= 0.6 * target_s or n >= S:
+            break
+        n = int(min(S, max(2 * n, n * target_s / max(dt, 1e-3))))
+        dt, fl = oracle_sample(q, k, v, dout, causal, scale, pick_rows(S, n, seed=2))
     return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": oracle.threads(), "kind": "oracle",
             "sample": (f"fp64 CPU oracle, head (0,0) of {WORKLOAD['name']} "
                        f"{'causal' if causal else 'non-causal'}: forward, backward row "

@@ -77,6 +77,8 @@ struct BwdCfg {
     static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, true, true);      // dQ
 };
 
+__device__ __forceinline__ int nT_of(int U, int BH) { return U / BH; }
+
 struct BUnit {
     int bh;  // b * H + h
     int j;   // key tile; -1 = no unit for this CTA this round
@@ -92,8 +94,11 @@ __device__ __forceinline__ bool bunit_at(int it, int U, int BH, BUnit &out) {
         out.j = -1;
         return true;
     }
-    out.bh = u % BH;
-    out.j = u / BH;  // key tile 0 first: under a causal mask it has the most blocks
+    // key tiles of one head are consecutive (concurrent CTAs share that head's
+    // Q, dO and dQ accumulator in L2); within a head key tile 0 comes first,
+    // which under a causal mask is the one with the most query blocks
+    out.bh = u / nT_of(U, BH);
+    out.j = u % nT_of(U, BH);
     return true;
 }
 

@@ -70,11 +70,13 @@ struct Unit {
     int p;   // query rows [256p, 256p + 256); -1: no unit for this CTA this round
 };
 
-// Work-unit order.  Units are numbered longest-first (p descending, which is
-// the order of decreasing work under a causal mask) with the head index
-// fastest; CTAs take them in a serpentine round-robin, which balances the
-// triangular causal work like an LPT list schedule.  Returns false when the
-// CTA has no further rounds.
+// Work-unit order.  Units are numbered longest-first over the whole launch (p
+// descending, which is the order of decreasing work under a causal mask) with
+// the head index fastest; CTAs take them in a serpentine round-robin, which
+// balances the triangular causal work like an LPT list schedule.  (Keeping
+// concurrent CTAs on one head instead measured 10 % slower for causal masks
+// on GB300 and no faster without.)  Returns false when the CTA has no further
+// rounds.
 __device__ __forceinline__ bool unit_at(int it, int U, int BH, int P, Unit &out) {
     const int G = gridDim.x;
     const int base = it * G;

@@ -262,7 +262,6 @@ fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float 
     if (poly_exp2_groups != 0 && poly_exp2_groups != 1 && poly_exp2_groups != 2 &&
         poly_exp2_groups != 8)
         return FA_ERR_INVALID_ARG;
-    if (D == 256) return FA_ERR_UNSUPPORTED;
     const DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != FA_OK) return st;
     if ((st = get_encoder()) != FA_OK) return st;

@@ -52,8 +52,12 @@ template <int D>
 struct FwdCfg {
     static constexpr int kBoxes = D / 64;                // TMA boxes per 128-row tile
     static constexpr int kTileBytes = kBox * kBoxes;     // 128 x D bf16
-    static constexpr int kStages = (D == 64) ? 8 : 4;    // ring slots (one K or V tile each)
-    static constexpr int kQBytes = 2 * kTileBytes;
+    // query tiles per CTA: two ping-pong tiles, except at D = 256 where two O
+    // accumulators (2 x 256 columns) and two S tiles exceed Tensor Memory
+    static constexpr int kNQ = (D == 256) ? 1 : 2;
+    static constexpr int kRows = kBlockM * kNQ;          // query rows per work unit
+    static constexpr int kStages = (D == 64) ? 8 : (D == 128 ? 4 : 2);  // ring slots
+    static constexpr int kQBytes = kNQ * kTileBytes;
     static constexpr int kRingOff = kQBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
     // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int lane = threadIdx.x & 31;
     const int H = args.H, S = args.S;
     const int BH = args.B * H;
-    const int P = (S + 2 * kBlockM - 1) / (2 * kBlockM);
+    const int P = (S + Cfg::kRows - 1) / Cfg::kRows;
     const int U = BH * P;
     const int nKV = (S + kBlockN - 1) / kBlockN;
 
@@ -171,10 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t smem_base = smem_u32(smem);
 
     // key tiles visited by query tile 0 / 1 of unit p
+    // (with a single query tile, n1 = n0)
     auto tiles_for = [&](int p, int &n0, int &n1) {
         if (args.causal) {
-            n0 = min(2 * p * kBlockM + kBlockM - 1, S - 1) / kBlockN + 1;
-            n1 = min(2 * p * kBlockM + 2 * kBlockM - 1, S - 1) / kBlockN + 1;
+            n0 = min(p * Cfg::kRows + kBlockM - 1, S - 1) / kBlockN + 1;
+            n1 = min(p * Cfg::kRows + Cfg::kNQ * kBlockM - 1, S - 1) / kBlockN + 1;
         } else {
             n0 = n1 = nKV;
         }
@@ -197,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 if (!mbar_wait(q_empty, (qi & 1) ^ 1, w)) { ok = false; break; }
                 ++qi;
                 mbar_arrive_expect_tx(q_full, Cfg::kQBytes);
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < Cfg::kNQ; ++t)
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_4d(smem + t * Cfg::kTileBytes + c * kBox, &args.tm_q, q_full,
-                                    64 * c, h, 2 * un.p * kBlockM + t * kBlockM, b);
+                                    64 * c, h, un.p * Cfg::kRows + t * kBlockM, b);
                 for (int j = 0; j < n1 && ok; ++j) {
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t slot = ring % Cfg::kStages;
@@ -254,8 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 tc_fence_after();
                 issue_qk<D>(tS0, q0, ring_base + kslot * Cfg::kTileBytes);
                 mma_commit(&s_full[0]);
-                issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
-                mma_commit(&s_full[1]);
+                if constexpr (Cfg::kNQ == 2) {
+                    issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
+                    mma_commit(&s_full[1]);
+                }
                 mma_commit(&kv_empty[kslot]);
                 for (int j = 0; j < n1; ++j) {
                     const uint32_t vslot = ring % Cfg::kStages;
@@ -278,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         pph0 ^= 1;
                         tc_fence_after();
                         issue_pv<D>(tO0, tS0, vaddr, j > 0);
+                        if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[vslot]);
                         if (j + 1 < n0) {
                             w.code = kErrFwdWait + 14;
                             if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
@@ -285,10 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                             tc_fence_after();
                             issue_qk<D>(tS0, q0, naddr);
                             mma_commit(&s_full[0]);
+                            if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[nslot]);
                         } else {
                             mma_commit(&o_full[0]);
+                            if constexpr (Cfg::kNQ == 1) mma_commit(q_empty);
                         }
                     }
+                    if constexpr (Cfg::kNQ == 1) continue;
                     w.code = kErrFwdWait + 15;
                     if (!mbar_wait(&p_full[1], pph1, w)) { ok = false; break; }
                     pph1 ^= 1;
@@ -316,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax + epilogue
-        const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+        const int t = (warp - 4) >> 2;  // query tile of this warpgroup (idle if t >= kNQ)
         const int quarter = warp & 3;   // TMEM lane quarter this warp may access
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -326,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const float tau = args.rescale_threshold;
         WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 20 + t};
         uint32_t sph = 0, oph = 0;
-        bool ok = true;
+        bool ok = (t < Cfg::kNQ);
         for (int it = 0; ok; ++it) {
             Unit un;
             if (!unit_at(it, U, BH, P, un)) break;
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             int n0, n1;
             tiles_for(un.p, n0, n1);
             const int n = t ? n1 : n0;
-            const int row = 2 * un.p * kBlockM + t * kBlockM + r_in_tile;
+            const int row = un.p * Cfg::kRows + t * kBlockM + r_in_tile;
             float m_used = -INFINITY;  // reference maximum, log2 units of scaled scores
             float l = 0.f;             // running row sum relative to m_used
             for (int j = 0; j < n; ++j) {
@@ -468,7 +479,7 @@ cudaError_t launch_fwd_inst(const FwdArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const long long P = (a.S + 255) / 256;
+    const long long P = (a.S + Cfg::kRows - 1) / Cfg::kRows;
     const long long U = static_cast<long long>(a.B) * a.H * P;
     const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
     kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
@@ -492,6 +503,7 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     switch (a.D) {
         case 64: return launch_fwd_d<64>(a, stream);
         case 128: return launch_fwd_d<128>(a, stream);
+        case 256: return launch_fwd_d<256>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -29,9 +29,17 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.where(ax > 0, 2.0 ** (e - 8), 0.0)
 
 
-def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None):
+def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None, peaked=False):
     """Compare GPU o [B,S,H,D] / lse [B,H,S] with the oracle on the listed
-    heads (and rows).  Returns (max O error, max LSE error)."""
+    heads (and rows).  Returns (max O error, max LSE error).
+
+    peaked=True (the stress inputs: scores ~30x the N(0,1) scale, nearly
+    one-hot rows): P enters the PV product rounded to bf16 (relative 2^-9,
+    FlashAttention-4 pages: bf16 quantisation dominates), which alone can move
+    O by up to 2^-9 max|V|; with the output's own half-ulp that can exceed the
+    plain gate.  The bound asserted is then 1e-2 + ulp/2 + 2^-8 max|V| (the
+    P-rounding bound with a factor 2 for the fp32 products around it), and at
+    most 1e-5 of the elements may exceed the plain gate."""
     ref = oracle.forward(q, k, v, causal, scale, heads=heads, rows=rows)
     o_cpu = o.float().cpu()
     lse_cpu = lse.cpu()
@@ -46,6 +54,12 @@ def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None):
             lg = lse_cpu[b, h, idx].double().numpy()
         err = np.abs(og - o_ref)
         tol = O_ATOL + half_ulp_bf16(o_ref)
+        if peaked:
+            vmax = float(np.abs(_f64_head(v, b, h)).max())
+            over = int((err > tol).sum())
+            assert over <= max(1, int(1e-5 * err.size)), (
+                f"{over} of {err.size} O elements above the plain gate in head {(b, h)}")
+            tol = tol + 2.0 ** -8 * vmax
         bad = err > tol
         assert not bad.any(), (
             f"O mismatch head {(b, h)}: max err {err.max():.4g}, "
@@ -55,6 +69,10 @@ def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None):
         worst_o = max(worst_o, float(err.max()))
         worst_l = max(worst_l, float(lerr.max()))
     return worst_o, worst_l
+
+
+def _f64_head(x, b, h):
+    return x[b, :, h].double().numpy()
 
 
 def rel_l2(got: np.ndarray, want: np.ndarray) -> float:

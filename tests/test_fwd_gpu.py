@@ -31,7 +31,7 @@ def test_small_config_all_heads(causal):
     check_forward(q, k, v, o, lse, causal, scale, heads=None)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("S", [1, 2, 127, 128, 129, 255, 256, 257, 300, 511, 640])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_lengths(S, D, causal):
@@ -63,7 +63,7 @@ def test_long_context_b1_h16_s32768_d128_sampled_rows(causal):
     check_forward(q, k, v, o, lse, causal, scale, heads=[(0, 0), (0, 15)], rows=rows)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("S,B", [(1024, 16), (4096, 4), (16384, 1)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_stress_sweep(S, B, D, causal):
@@ -71,7 +71,8 @@ def test_stress_sweep(S, B, D, causal):
     # conditional rescale fires
     q, k, v, o, lse, scale = _run(B, 16, S, D, causal, stress=True)
     rows = None if S <= 4096 else sample_rows(S, 128, seed=2)
-    check_forward(q, k, v, o, lse, causal, scale, heads=[(0, 0), (B - 1, 15)], rows=rows)
+    check_forward(q, k, v, o, lse, causal, scale, heads=[(0, 0), (B - 1, 15)], rows=rows,
+                  peaked=True)
 
 
 @pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
@@ -81,11 +82,19 @@ def test_numerics_knobs_do_not_change_result(tau, groups):
     # only, mixed, or polynomial only
     q, k, v, o, lse, scale = _run(2, 4, 1024, 128, True, stress=True,
                                   rescale_threshold=tau, poly_exp2_groups=groups)
-    check_forward(q, k, v, o, lse, True, scale, heads=[(0, 0), (1, 3)])
+    check_forward(q, k, v, o, lse, True, scale, heads=[(0, 0), (1, 3)], peaked=True)
     _, _, _, o_ref, lse_ref, _ = _run(2, 4, 1024, 128, True, stress=True,
                                       rescale_threshold=0.0, poly_exp2_groups=0)
     assert (o.float() - o_ref.float()).abs().max().item() <= 2e-2
     assert (lse - lse_ref).abs().max().item() <= 1e-3
+
+
+@pytest.mark.parametrize("D", [64, 256])
+@pytest.mark.parametrize("groups", [0, 2])
+def test_numerics_knobs_other_head_dims(D, groups):
+    q, k, v, o, lse, scale = _run(1, 3, 700, D, True, stress=True, rescale_threshold=0.0,
+                                  poly_exp2_groups=groups)
+    check_forward(q, k, v, o, lse, True, scale, heads=None, peaked=True)
 
 
 def test_deterministic_repeat():

@@ -204,19 +204,30 @@ def run_step(buf, causal, scale, ev=None):
 
 
 def barrier(dist_on):
+    """All ranks meet, and this rank's GPU work is finished."""
     if dist_on:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x, dist_on):
+    """The largest value of x over all ranks (the step time that counts)."""
     if not dist_on:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(world, flops_per_rank, ms_max):
+    """Whole-job throughput: every rank processes its own batch (weak
+    scaling), so the job does world x the per-rank FLOPs in the slowest
+    rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 def time_device(buf, causal, scale, steps, warmup, dist_on):
@@ -400,7 +411,7 @@ def main():
 
     ff, fb = flops(B, H, S, D, False)
     ffc, fbc = flops(B, H, S, D, True)
-    value = world * (ff + fb) / (ms * 1e-3) / 1e12
+    value = job_tflops(world, ff + fb, ms)
     fwd_tf, bwd_tf = ff / (fwd_ms * 1e-3) / 1e12, fb / (bwd_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     if bwd_ms >= fwd_ms:
@@ -423,13 +434,13 @@ def main():
         "fwd_pct_of_2250": 100 * fwd_tf / NOMINAL_PEAK_TFLOPS,
         "bwd_pct_of_2250": 100 * bwd_tf / NOMINAL_PEAK_TFLOPS,
         "pct_of_2250": 100 * value / world / NOMINAL_PEAK_TFLOPS,
-        "causal": {"tflops": world * (ffc + fbc) / (ms_c * 1e-3) / 1e12, "ms_per_step": ms_c,
+        "causal": {"tflops": job_tflops(world, ffc + fbc, ms_c), "ms_per_step": ms_c,
                    "fwd_tflops": ffc / (fwd_ms_c * 1e-3) / 1e12,
                    "bwd_tflops": fbc / (bwd_ms_c * 1e-3) / 1e12},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} bf16_tflops_sustained", "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic},
-        "e2e": {"value": world * (ff + fb) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+        "e2e": {"value": job_tflops(world, ff + fb, e2e_ms), "unit": "TFLOPS",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 4 * args.steps,  # fa_fwd 1 + fa_bwd 3 per step of the value's region
         "clocks": clocks,

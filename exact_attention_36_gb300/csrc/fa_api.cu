@@ -90,11 +90,12 @@ fa_status get_encoder() {
 // Tensor map over a bf16 [B,S,H,D] tensor: dims (D, H, S, B), box
 // 64 x 1 x 128 x 1 (a 128-row x 128-byte tile), 128-byte swizzle, zero fill
 // outside the tensor (ragged sequence tails read as zeros).
-fa_status make_map_bshd(CUtensorMap *m, const void *ptr, int B, int S, int H, int D) {
+fa_status make_map_bshd(CUtensorMap *m, const void *ptr, int B, int S, int H, int D,
+                        unsigned box_rows = 128) {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
                                    (cuuint64_t)S * H * D * 2};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t box[4] = {64, 1, box_rows, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -110,10 +111,10 @@ fa_status make_map_bshd(CUtensorMap *m, const void *ptr, int B, int S, int H, in
 // Tensor map over the fp32 dQ accumulator viewed as [B*H][S][D]: box
 // 32 x 128 x 1 (128 rows x 128 bytes), 128-byte swizzle; rows past S are
 // outside the tensor, so reductions into them are dropped.
-fa_status make_map_dqacc(CUtensorMap *m, void *ptr, int BH, int S, int D) {
+fa_status make_map_dqacc(CUtensorMap *m, void *ptr, int BH, int S, int D, unsigned box_rows) {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)S * D * 4};
-    const cuuint32_t box[3] = {32, 128, 1};
+    const cuuint32_t box[3] = {32, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -313,11 +314,13 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     if ((st = get_encoder()) != FA_OK) return st;
     fa::BwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D)) != FA_OK) return st;
+    // D = 256 streams 64-query blocks and stages dQ as 32 x 32 tiles
+    const unsigned qrows = D == 256 ? 64 : 128, dqrows = D == 256 ? 32 : 128;
+    if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_do, dout, B, S, H, D)) != FA_OK) return st;
-    if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, B * H, S, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_do, dout, B, S, H, D, qrows)) != FA_OK) return st;
+    if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, B * H, S, D, dqrows)) != FA_OK) return st;
     a.o = o;
     a.dout = dout;
     a.lse = lse;

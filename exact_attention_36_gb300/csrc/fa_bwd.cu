@@ -671,6 +671,16 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
     switch (a.D) {
         case 64: return launch_bwd_d<64>(a, stream);
         case 128: return launch_bwd_d<128>(a, stream);
+        case 256: {
+            const long long rows = static_cast<long long>(a.B) * a.H * a.S;
+            const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+            fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(a);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            if ((e = launch_bwd_main_d256(a, stream)) != cudaSuccess) return e;
+            fa_bwd_dq_cvt<256><<<blocks, 256, 0, stream>>>(a);
+            return cudaGetLastError();
+        }
         default: return cudaErrorNotSupported;
     }
 }

@@ -1,0 +1,483 @@
+// fa_bwd_d256.cu -- fused attention backward main kernel for head dim 256.
+//
+// Same mathematics as fa_bwd.cu ("FlashAttention-4: Algorithm and Kernel
+// Pipelining Co-Design for Asymmetric Hardware Scaling" (gist.science/nl),
+// Technische samenvatting, Methodologie §3), reorganised so that it fits the
+// Tensor Memory and shared memory of one SM at D = 256:
+//   * dK and dV for all 256 columns would fill the 512 TMEM columns by
+//     themselves, so a work unit is (b, h, key tile j of 128 keys, output
+//     half oh): it accumulates dK[:, 128oh : 128oh+128] and the same half of
+//     dV, and adds the same half of dQ.  S^T and dP^T (contractions over all
+//     256 columns) are recomputed by both halves.
+//   * K_j and V_j (64 KB each) stay resident; queries stream in blocks of 64
+//     rows (Q_i and dO_i 32 KB each, one stage each).
+//   * dQ^T = K_j[:, half]^T dS^T is formed with the head dim on the TMEM
+//     lanes (M = 128), so the drain warps hold one dQ column each.
+// Tensor Memory: X = S^T / P^T (64 cols) | Y = dP^T / dS^T / dQ^T (64 cols) |
+// dV half (128) | dK half (128).  The MMAs of a block run in order
+// S, dP, dV, dK, dQ; this variant does not overlap blocks.
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kKeys = 128;     // keys per unit
+constexpr int kQB = 64;        // queries per block
+constexpr int kD = 256;
+constexpr int kBoxK = 16384;   // K/V box: 128 rows x 64 bf16
+constexpr int kBoxQ = 8192;    // Q/dO box: 64 rows x 64 bf16
+
+struct Cfg {
+    static constexpr int kOffK = 0;                   // 4 boxes
+    static constexpr int kOffV = kOffK + 4 * kBoxK;   // 4 boxes
+    static constexpr int kOffQ = kOffV + 4 * kBoxK;   // 4 boxes (64 rows)
+    static constexpr int kOffDO = kOffQ + 4 * kBoxQ;  // 4 boxes
+    static constexpr int kOffDS = kOffDO + 4 * kBoxQ; // 128 keys x 64 queries bf16 (16 KB)
+    static constexpr int kOffRed = kOffDS + 16384;    // 2 x (64 rows x 32 fp32) dQ staging
+    static constexpr int kOffStat = kOffRed + 16384;  // 64 lse2 + 64 delta
+    static constexpr int kOffBar = kOffStat + 512;
+    static constexpr int kNumBars = 15;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked)
+    static constexpr uint32_t kTX = 0, kTY = 64, kTdV = 128, kTdK = 256;
+    static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, kQB, false, false);   // S^T, dP^T
+    static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, 128, false, true);   // dV, dK half
+    static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, kQB, true, true);     // dQ^T half
+};
+static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
+
+struct Unit256 {
+    int bh, j, oh;  // j = -1: no unit for this CTA this round
+};
+
+__device__ __forceinline__ bool unit256_at(int it, int U, int nT, Unit256 &out) {
+    const int G = gridDim.x;
+    const int base = it * G;
+    if (base >= U) return false;
+    const int c = (it & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int u = base + c;
+    if (u >= U) {
+        out.j = -1;
+        return true;
+    }
+    // the two halves of a key tile, then the key tiles of a head, are adjacent
+    out.oh = u & 1;
+    out.j = (u >> 1) % nT;
+    out.bh = (u >> 1) / nT;
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_constant__ BwdArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) atomicCAS(args.err_word, 0, kErrBwdWait + 0xfe);
+        return;
+    }
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1;
+    uint64_t *q_full = bars + 2, *q_empty = bars + 3;
+    uint64_t *do_full = bars + 4, *do_empty = bars + 5;
+    uint64_t *s_full = bars + 6, *dp_full = bars + 7;
+    uint64_t *p_ready = bars + 8, *ds_ready = bars + 9;
+    uint64_t *dq_full = bars + 10, *dq_empty = bars + 11;
+    uint64_t *dkdv_full = bars + 12, *dkdv_empty = bars + 13;
+    uint64_t *drain = bars + 14;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
+    float *stat = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // lse2[64] | delta[64]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = args.H, S = args.S;
+    const int BH = args.B * H;
+    const int nT = (S + kKeys - 1) / kKeys;  // key tiles
+    const int nQ = (S + kQB - 1) / kQB;      // query blocks
+    const int U = BH * nT * 2;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        mbar_init(q_full, 2);  // TMA + LSE/Delta written
+        mbar_init(q_empty, 1);
+        mbar_init(do_full, 1);
+        mbar_init(do_empty, 1);
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_ready, 128);
+        mbar_init(ds_ready, 128);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 128);
+        mbar_init(dkdv_full, 1);
+        mbar_init(dkdv_empty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t sbase = smem_u32(smem);
+    // first query block a key tile sees (causal: queries >= first key)
+    auto first_qblock = [&](int j) { return args.causal ? (j * kKeys) / kQB : 0; };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x51};
+        const float log2e = 1.4426950408889634f;
+        uint32_t nunit = 0, n = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            Unit256 un;
+            if (!unit256_at(it, U, nT, un)) break;
+            if (un.j < 0) continue;
+            const int b = un.bh / H, h = un.bh % H;
+            if (lane == 0) {
+                w.code = kErrBwdWait + 0x51;
+                ok = mbar_wait(kv_empty, (nunit & 1) ^ 1, w);
+                if (ok) {
+                    mbar_arrive_expect_tx(kv_full, 8 * kBoxK);
+                    for (int c = 0; c < 4; ++c) {
+                        tma_load_4d(smem + Cfg::kOffK + c * kBoxK, &args.tm_k, kv_full, 64 * c, h,
+                                    un.j * kKeys, b);
+                        tma_load_4d(smem + Cfg::kOffV + c * kBoxK, &args.tm_v, kv_full, 64 * c, h,
+                                    un.j * kKeys, b);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            ++nunit;
+            for (int i = first_qblock(un.j); i < nQ && ok; ++i, ++n) {
+                w.code = kErrBwdWait + 0x52;
+                ok = mbar_wait(q_empty, (n & 1) ^ 1, w);
+                ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, 4 * kBoxQ);
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_4d(smem + Cfg::kOffQ + c * kBoxQ, &args.tm_q, q_full, 64 * c, h,
+                                    i * kQB, b);
+                }
+                const size_t rbase = static_cast<size_t>(un.bh) * S;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int qr = r * 32 + lane;
+                    const int q = i * kQB + qr;
+                    stat[qr] = q < S ? args.lse[rbase + q] * log2e : INFINITY;
+                    stat[64 + qr] = q < S ? args.delta[rbase + q] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(q_full);
+                    w.code = kErrBwdWait + 0x53;
+                    ok = mbar_wait(do_empty, (n & 1) ^ 1, w);
+                    if (ok) {
+                        mbar_arrive_expect_tx(do_full, 4 * kBoxQ);
+                        for (int c = 0; c < 4; ++c)
+                            tma_load_4d(smem + Cfg::kOffDO + c * kBoxQ, &args.tm_do, do_full,
+                                        64 * c, h, i * kQB, b);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            }
+        }
+        if (!ok && lane == 0) {
+            if (nunit > 0) mbar_wait_drain(kv_full, (nunit - 1) & 1);
+            if (n > 0) {
+                mbar_wait_drain(q_full, (n - 1) & 1);
+                mbar_wait_drain(do_full, (n - 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x60};
+            const uint32_t tX = tmem + Cfg::kTX, tY = tmem + Cfg::kTY;
+            const uint32_t tdV = tmem + Cfg::kTdV, tdK = tmem + Cfg::kTdK;
+            const uint32_t aK = sbase + Cfg::kOffK, aV = sbase + Cfg::kOffV;
+            const uint32_t aQ = sbase + Cfg::kOffQ, aDO = sbase + Cfg::kOffDO;
+            const uint32_t aDS = sbase + Cfg::kOffDS;
+            uint32_t nunit = 0, n = 0;
+            bool ok = true;
+#define FA_WAIT(bar, par, site)                                  \
+    do {                                                         \
+        w.code = kErrBwdWait + (site);                           \
+        if (!mbar_wait((bar), (par), w)) { ok = false; break; } \
+    } while (0)
+            for (int it = 0; ok; ++it) {
+                Unit256 un;
+                if (!unit256_at(it, U, nT, un)) break;
+                if (un.j < 0) continue;
+                FA_WAIT(kv_full, nunit & 1, 0x60);
+                if (!ok) break;
+                const int i0 = first_qblock(un.j);
+                for (int i = i0; i < nQ; ++i, ++n) {
+                    FA_WAIT(q_full, n & 1, 0x61);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        mma_ss(tX, sdesc_sw128(aK + (kk / 4) * kBoxK + (kk % 4) * 32, 16, 1024),
+                               sdesc_sw128(aQ + (kk / 4) * kBoxQ + (kk % 4) * 32, 16, 1024),
+                               Cfg::kIdescSS, kk > 0 ? 1u : 0u);
+                    mma_commit(s_full);
+                    if (n > 0) {
+                        FA_WAIT(dq_empty, (n - 1) & 1, 0x62);  // the drain has read dQ(n-1)
+                        if (!ok) break;
+                    }
+                    FA_WAIT(do_full, n & 1, 0x63);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        mma_ss(tY, sdesc_sw128(aV + (kk / 4) * kBoxK + (kk % 4) * 32, 16, 1024),
+                               sdesc_sw128(aDO + (kk / 4) * kBoxQ + (kk % 4) * 32, 16, 1024),
+                               Cfg::kIdescSS, kk > 0 ? 1u : 0u);
+                    mma_commit(dp_full);
+                    FA_WAIT(p_ready, n & 1, 0x64);
+                    if (!ok) break;
+                    if (i == i0 && nunit > 0) {
+                        FA_WAIT(dkdv_empty, (nunit - 1) & 1, 0x65);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    const bool acc = (i > i0);
+                    // dV[:, half] += P^T dO_i[:, half]   (B MN-major, 2 boxes of 64 columns)
+#pragma unroll
+                    for (int kk = 0; kk < kQB / 16; ++kk)
+                        mma_ts(tdV, tX + kk * 8,
+                               sdesc_sw128(aDO + 2 * un.oh * kBoxQ + kk * 2048, kBoxQ, 1024),
+                               Cfg::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+                    mma_commit(do_empty);
+                    FA_WAIT(ds_ready, n & 1, 0x66);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kQB / 16; ++kk)
+                        mma_ts(tdK, tY + kk * 8,
+                               sdesc_sw128(aQ + 2 * un.oh * kBoxQ + kk * 2048, kBoxQ, 1024),
+                               Cfg::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+                    mma_commit(q_empty);
+                    // dQ^T[half] = K_j[:, half]^T dS^T -> Y (head dim on the lanes)
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk)
+                        mma_ss(tY, sdesc_sw128(aK + 2 * un.oh * kBoxK + kk * 2048, kBoxK, 1024),
+                               sdesc_sw128(aDS + kk * 2048, kBoxK, 1024), Cfg::kIdescDQ,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(dq_full);
+                    if (i + 1 == nQ) {
+                        mma_commit(dkdv_full);
+                        mma_commit(kv_empty);
+                    }
+                }
+                ++nunit;
+            }
+#undef FA_WAIT
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    }
+    else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P^T and dS^T (lane = key)
+        const int quarter = warp & 3;
+        const int kr = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tX = tmem + Cfg::kTX + lane_off, tY = tmem + Cfg::kTY + lane_off;
+        const float c2 = args.scale_log2;
+        WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x70};
+        uint32_t n = 0;
+        bool ok = true;
+        uint8_t *ds_row = smem + Cfg::kOffDS + kr * 128;
+        for (int it = 0; ok; ++it) {
+            Unit256 un;
+            if (!unit256_at(it, U, nT, un)) break;
+            if (un.j < 0) continue;
+            const int key = un.j * kKeys + kr;
+            for (int i = first_qblock(un.j); i < nQ; ++i, ++n) {
+                w.code = kErrBwdWait + 0x70;
+                if (!mbar_wait(q_full, n & 1, w)) { ok = false; break; }
+                w.code = kErrBwdWait + 0x71;
+                if (!mbar_wait(s_full, n & 1, w)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t pk[32];
+                {
+                    uint32_t sr[2][32];
+                    tmem_ld32(tX, sr[0]);
+                    tmem_ld32(tX + 32, sr[1]);
+                    tmem_ld_wait(sr[0]);
+                    tmem_ld_wait(sr[1]);
+                    const bool diag = args.causal && (i * kQB < (un.j + 1) * kKeys);
+                    if (diag || (un.j + 1) * kKeys > S) {
+                        const bool key_ok = key < S;
+                        const int q0 = i * kQB;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (!key_ok || (diag && q0 + c * 32 + e < key))
+                                    sr[c][e] = __float_as_uint(-INFINITY);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = ex2_mufu(fmaf(__uint_as_float(sr[c][e]), c2, -stat[c * 32 + e]));
+                            const float p1 =
+                                ex2_mufu(fmaf(__uint_as_float(sr[c][e + 1]), c2, -stat[c * 32 + e + 1]));
+                            pk[(c * 32 + e) / 2] = pack_bf16x2(p0, p1);
+                        }
+                }
+                tmem_st16(tX, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tX + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_ready);
+                w.code = kErrBwdWait + 0x72;
+                if (!mbar_wait(dp_full, n & 1, w)) { ok = false; break; }
+                if (n > 0) {
+                    w.code = kErrBwdWait + 0x73;  // dQ MMA of the previous block has read dS
+                    if (!mbar_wait(dq_full, (n - 1) & 1, w)) { ok = false; break; }
+                }
+                tc_fence_after();
+                uint32_t dr[2][32];
+                tmem_ld32(tY, dr[0]);
+                tmem_ld32(tY + 32, dr[1]);
+                tmem_ld_wait(dr[0]);
+                tmem_ld_wait(dr[1]);
+                uint32_t dsw[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int col = c * 32 + e;
+                        const uint32_t pw = pk[col >> 1];
+                        const float d0 = __uint_as_float(pw << 16) *
+                                         (__uint_as_float(dr[c][e]) - stat[64 + col]);
+                        const float d1 = __uint_as_float(pw & 0xffff0000u) *
+                                         (__uint_as_float(dr[c][e + 1]) - stat[64 + col + 1]);
+                        dsw[col >> 1] = pack_bf16x2(d0, d1);
+                    }
+                tmem_st16(tY, *reinterpret_cast<uint32_t(*)[16]>(&dsw[0]));
+                tmem_st16(tY + 16, *reinterpret_cast<uint32_t(*)[16]>(&dsw[16]));
+                // shared copy (MN-major B of the dQ MMA): this key's 64 queries,
+                // 128-byte row, 128B swizzle
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(ds_row + ((ch ^ (kr & 7)) << 4)) =
+                        make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
+                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(ds_ready);
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        // dQ^T rows (lane = head-dim column d of the half) are staged per warp
+        // as 32 queries x 32 columns (4 KB, 128B swizzle) and added into the
+        // accumulator with TMA bulk reductions issued by the warp's lane 0.
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint8_t *stage = smem + Cfg::kOffRed + quarter * 4096;
+        WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x80};
+        uint32_t n = 0, nunit = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            Unit256 un;
+            if (!unit256_at(it, U, nT, un)) break;
+            if (un.j < 0) continue;
+            const int b = un.bh / H, h = un.bh % H;
+            for (int i = first_qblock(un.j); i < nQ; ++i, ++n) {
+                w.code = kErrBwdWait + 0x80;
+                if (!mbar_wait(dq_full, n & 1, w)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t col[2][32];  // dQ^T[d][query] for 64 queries
+                tmem_ld32(tmem + Cfg::kTY + lane_off, col[0]);
+                tmem_ld32(tmem + Cfg::kTY + lane_off + 32, col[1]);
+                tmem_ld_wait(col[0]);
+                tmem_ld_wait(col[1]);
+                tc_fence_before();
+                mbar_arrive(dq_empty);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (lane == 0) bulk_wait_read<0>();  // previous reduction has read `stage`
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        *reinterpret_cast<float *>(stage + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) +
+                                                   (lane & 3) * 4) = __uint_as_float(col[half][q]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_3d(&args.tm_dqacc, stage, un.oh * 128 + quarter * 32,
+                                          i * kQB + half * 32, un.bh);
+                        bulk_commit();
+                    }
+                }
+            }
+            if (!ok) break;
+            w.code = kErrBwdWait + 0x81;
+            if (!mbar_wait(dkdv_full, nunit & 1, w)) { ok = false; break; }
+            ++nunit;
+            tc_fence_after();
+            const int key = un.j * kKeys + r;  // dK / dV lanes are keys
+            const size_t orow = ((static_cast<size_t>(b) * S + key) * H + h) * kD + un.oh * 128;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
+                const float mul = which ? args.scale : 1.f;
+                uint16_t *out = reinterpret_cast<uint16_t *>(which ? args.dk : args.dv) + orow;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tsrc + c * 32, v);
+                    tmem_ld_wait(v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
+                                            __uint_as_float(v[2 * e + 1]) * mul);
+                    if (key < S) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                 pk[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(dkdv_empty);
+        }
+        if (lane == 0) bulk_wait<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_d256(const BwdArgs &a, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel_d256,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kKeys - 1) / kKeys) * 2;
+    const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
+    fa_bwd_kernel_d256<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

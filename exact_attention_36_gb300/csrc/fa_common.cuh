@@ -30,7 +30,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [B,S,H,D], same boxes as the forward
-    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 128 x 1, 128B swizzle
+    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 128 x 1 (D = 256: 32 x 32 x 1)
     const void *o, *dout;                 // bf16 [B,S,H,D]
     const float *lse;                     // fp32 [B,H,S]
     float *dq_acc;                        // fp32 [B,H,S,D]
@@ -48,5 +48,8 @@ struct BwdArgs {
 // launch (cudaSuccess when enqueued).
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream);
+// main backward kernel for D = 256 (fa_bwd_d256.cu); Q/dO tensor maps with
+// 64-row boxes and a dQ-accumulator map with 32 x 32 boxes
+cudaError_t launch_bwd_main_d256(const BwdArgs &a, cudaStream_t stream);
 
 }  // namespace fa

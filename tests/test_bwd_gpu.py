@@ -31,7 +31,7 @@ def test_small_config_all_heads(causal):
     check_backward(q, k, v, do, dq, dk, dv, causal, scale, heads=None)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("S", [1, 2, 100, 127, 128, 129, 255, 300, 640])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_lengths(S, D, causal):
@@ -66,7 +66,7 @@ def test_long_context_b1_h16_s32768_d128_sampled(causal):
     _invariants(do, dk, dv)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("S,B", [(1024, 16), (4096, 4), (16384, 1)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_stress_sweep(S, B, D, causal):

@@ -301,9 +301,13 @@ size_t fa_bwd_workspace_size(int B, int H, int S, int D) {
     return round256(n * D * sizeof(float)) + round256(n * sizeof(float));
 }
 
-fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
-                 const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
-                 int B, int H, int S, int D, int causal, float scale, void *stream) {
+}  // extern "C"
+
+namespace {
+// fa_bwd and fa_bwd_deterministic; sem == nullptr selects the atomic-order dQ.
+fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, float *dq_acc, float *delta, int *sem, void *dq, void *dk,
+                   void *dv, int B, int H, int S, int D, int causal, float scale, void *stream) {
     const void *ptrs[11] = {q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv};
     for (const void *p : ptrs)
         if (!p || !aligned16(p)) return FA_ERR_INVALID_ARG;
@@ -326,6 +330,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     a.lse = lse;
     a.dq_acc = dq_acc;
     a.delta = delta;
+    a.dq_sem = sem;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -342,6 +347,31 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
+                 int B, int H, int S, int D, int causal, float scale, void *stream) {
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, B, H, S, D,
+                    causal, scale, stream);
+}
+
+size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D) {
+    if (check_shape(B, H, S, D, 1.f) != FA_OK) return 0;
+    const size_t n = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 63) / 64);
+    return (n * sizeof(int) + 255) & ~static_cast<size_t>(255);
+}
+
+fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                               const void *dout, const float *lse, float *dq_acc, float *delta,
+                               int *dq_sem, void *dq, void *dk, void *dv, int B, int H, int S,
+                               int D, int causal, float scale, void *stream) {
+    if (!dq_sem || !aligned16(dq_sem)) return FA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, B, H, S, D,
+                    causal, scale, stream);
 }
 
 fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream) {

@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     const int BH = args.B * H;
     const int nT = (S + kBlk - 1) / kBlk;  // key tiles = query blocks
     const int U = BH * nT;
+    const int nSem = (S + 63) / 64;        // deterministic-mode counters per head
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -543,8 +544,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     fence_proxy_async_smem();
                     named_bar_sync(1, 128);
                     if (leader) {
-                        tma_reduce_add_3d(&args.tm_dqacc, buf, 32 * c, i * kBlk, un.bh);
-                        bulk_commit();
+                        // deterministic mode: key tile j adds its share of dQ block i
+                        // only after tiles 0 .. j-1 have (they are the only tiles
+                        // before it that see block i), so every sum runs in key order.
+                        // A tile only ever waits on a smaller unit index (an earlier
+                        // or concurrent unit), so the waits cannot form a cycle.
+                        int *sem = args.dq_sem ? args.dq_sem + static_cast<size_t>(un.bh) * nSem +
+                                                     (i * kBlk) / 64
+                                               : nullptr;
+                        bool go = true;
+                        if (sem && c == 0) {
+                            w.code = kErrBwdWait + 42;
+                            go = counter_wait_geq(sem, un.j, w);
+                            fence_proxy_async_global();
+                        }
+                        if (go && !*abort_flag) {
+                            tma_reduce_add_3d(&args.tm_dqacc, buf, 32 * c, i * kBlk, un.bh);
+                            bulk_commit();
+                        }
+                        if (sem && c == D / 32 - 1) {
+                            bulk_wait<0>();  // this block's reductions are done in L2
+                            fence_proxy_async_global();
+                            __threadfence();
+                            red_release_gpu_add(sem, 1);
+                        }
                     }
                 }
             }
@@ -619,7 +642,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdAr
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) args.delta[row] = acc;
+    if (lane == 0) {
+        args.delta[row] = acc;
+        if (args.dq_sem && (q & 63) == 0)
+            args.dq_sem[bh * ((S + 63) / 64) + q / 64] = 0;
+    }
     float4 *z = reinterpret_cast<float4 *>(args.dq_acc + static_cast<size_t>(row) * D);
 #pragma unroll
     for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -659,7 +686,16 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
     const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
+    if (a.dq_sem) {
+        // CTAs wait on one another's dQ counters: a cooperative launch
+        // guarantees they are all resident at once
+        void *params[] = {const_cast<BwdArgs *>(&a)};
+        e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid),
+                                        dim3(kThreads), params, Cfg::kSmemBytes, stream);
+        if (e != cudaSuccess) return e;
+    } else {
+        kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
     return cudaGetLastError();
@@ -672,6 +708,7 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
         case 64: return launch_bwd_d<64>(a, stream);
         case 128: return launch_bwd_d<128>(a, stream);
         case 256: {
+            if (a.dq_sem) return cudaErrorNotSupported;  // no ordered dQ at D = 256 yet
             const long long rows = static_cast<long long>(a.B) * a.H * a.S;
             const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
             fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(a);

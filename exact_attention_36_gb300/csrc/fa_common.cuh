@@ -35,6 +35,7 @@ struct BwdArgs {
     const float *lse;                     // fp32 [B,H,S]
     float *dq_acc;                        // fp32 [B,H,S,D]
     float *delta;                         // fp32 [B,H,S]
+    int *dq_sem;                          // deterministic mode: [B*H][ceil(S/64)] counters, else null
     void *dq, *dk, *dv;                   // bf16 [B,S,H,D]
     int B, H, S, D;
     int causal;

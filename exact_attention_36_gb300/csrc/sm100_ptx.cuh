@@ -122,6 +122,35 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) 
     return true;
 }
 
+// Global counter helpers for cross-CTA ordering (the CTAs of the launch are
+// co-resident: cooperative launch).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Wait (bounded, like mbar_wait) until *p >= target.
+__device__ __forceinline__ bool counter_wait_geq(const int *p, int target, const WaitCtx &w) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > FA_WAIT_LIMIT_NS) {
+            *w.abort_flag = 1;
+            atomicCAS(w.err_word, 0, w.code);
+            return false;
+        }
+    }
+}
+
 // ----------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {

@@ -50,13 +50,17 @@ def lib():
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp]
+        L.fa_bwd_deterministic.argtypes = [vp] * 12 + [i, i, i, i, i, f, vp]
+        L.fa_bwd_semaphore_bytes.argtypes = [i, i, i, i]
+        L.fa_bwd_semaphore_bytes.restype = ctypes.c_size_t
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_cuda_error.argtypes = [ctypes.POINTER(i)]
         L.fa_device_error.argtypes = [ctypes.POINTER(i), i]
         L.fa_exp2_eval.argtypes = [vp, vp, ll, i, vp]
         L.fa_exp2_sweep.argtypes = [f, f, i, vp, vp]
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_last_cuda_error", "fa_device_error",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_deterministic", "fa_last_cuda_error",
+                     "fa_device_error",
                      "fa_exp2_eval", "fa_exp2_sweep"):
             getattr(L, name).restype = i
         _lib = L
@@ -114,6 +118,21 @@ def bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal: bool, scale: f
     _check("fa_bwd", st)
 
 
+def bwd_deterministic(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, causal: bool,
+                      scale: float, stream=None):
+    """fa_bwd_deterministic on caller-provided tensors (fixed-order dQ)."""
+    B, S, H, D = q.shape
+    st = lib().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                    _ptr(dq_acc), _ptr(delta), _ptr(dq_sem), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), B, H, S, D, int(bool(causal)), float(scale),
+                                    _stream(stream))
+    _check("fa_bwd_deterministic", st)
+
+
+def bwd_semaphore_bytes(B: int, H: int, S: int, D: int) -> int:
+    return int(lib().fa_bwd_semaphore_bytes(B, H, S, D))
+
+
 # ---------------------------------------------------------------- tensor API
 
 
@@ -136,8 +155,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
 
 
 def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
-             stream=None):
-    """Exact attention backward.  Returns (dq, dk, dv), bf16 [B, S, H, D]."""
+             stream=None, deterministic: bool = False):
+    """Exact attention backward.  Returns (dq, dk, dv), bf16 [B, S, H, D].
+
+    deterministic=True sums dQ over key tiles in a fixed order, so repeated
+    calls give bitwise-identical results (dK and dV always are)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _check_bshd(name, t, q.shape)
     B, S, H, D = q.shape
@@ -151,7 +173,13 @@ def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
     dq_acc = ws[:acc_bytes].view(torch.float32)
     delta = ws[acc_bytes:acc_bytes + n * 4].view(torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal, scale, stream)
+    if deterministic:
+        sem = torch.empty(bwd_semaphore_bytes(B, H, S, D) // 4, dtype=torch.int32,
+                          device=q.device)
+        bwd_deterministic(q, k, v, o, dout, lse, dq_acc, delta, sem, dq, dk, dv, causal, scale,
+                          stream)
+    else:
+        bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal, scale, stream)
     return dq, dk, dv
 
 

@@ -115,6 +115,26 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  int B, int H, int S, int D, int causal, float scale, void *stream);
 
 /*
+ * Deterministic backward ([nl] Methodologie §3 and Belangrijkste Resultaten:
+ * a deterministic mode ordered by semaphores): the same results as fa_bwd,
+ * except that every element of dQ is summed over the key tiles in a fixed
+ * order (key tile 0, 1, 2, ...), so repeated calls on the same inputs give
+ * bitwise-identical dQ (dK and dV are already reduced in a fixed order).
+ * The key tile that contributes to a 128-query block next waits on a per-block
+ * counter; the kernel is launched cooperatively, so all its CTAs are resident
+ * while they wait on one another.
+ *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes (contents on
+ *            entry ignored; the first launch zeroes it).
+ * Other arguments, results and errors as fa_bwd.  D = 256 returns
+ * FA_ERR_UNSUPPORTED.
+ */
+size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D);
+fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                               const void *dout, const float *lse, float *dq_acc, float *delta,
+                               int *dq_sem, void *dq, void *dk, void *dv,
+                               int B, int H, int S, int D, int causal, float scale, void *stream);
+
+/*
  * Backward for callers that cannot allocate device memory: code that runs
  * where cudaMalloc is not allowed or not wanted (host callbacks, plug-ins
  * that only get their inputs and outputs from a host framework, tools that

@@ -250,33 +250,58 @@ def time_device(buf, causal, scale, steps, warmup, dist_on):
 
 
 def time_e2e(q, k, v, dout, buf, causal, scale, steps, warmup, dist_on):
-    """The same step through the C ABI with host buffers: every step copies
-    Q, K, V, dO from pinned host memory, runs fwd + bwd, and reads dQ, dK, dV
-    back.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    """The same step through the C ABI with host buffers.  Every step copies
+    its Q, K, V, dO from pinned host memory and reads its dQ, dK, dV back;
+    the copies run on a second stream, double-buffered, so step k+1's inputs
+    arrive while step k computes.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    dev = buf.q.device
     hin = [t.pin_memory() for t in (q, k, v, dout)]
-    hout = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
-    dins = [buf.q, buf.k, buf.v, buf.dout]
-    douts = [buf.dq, buf.dk, buf.dv]
+    hout = [[torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+            for _ in range(2)]
+    bufs = [buf, Buffers(q, k, v, dout, dev)]
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(2)]  # inputs of buffer b copied
+    done = [torch.cuda.Event() for _ in range(2)]   # step on buffer b computed
+    fetched = [torch.cuda.Event() for _ in range(2)]  # outputs of buffer b read back
 
-    def step():
-        for d, h in zip(dins, hin):
-            d.copy_(h, non_blocking=True)
-        run_step(buf, causal, scale)
-        for h, d in zip(hout, douts):
-            h.copy_(d, non_blocking=True)
+    def upload(b):
+        with torch.cuda.stream(copy):
+            copy.wait_event(done[b])  # the previous step on this buffer finished with it
+            for d, h in zip((bufs[b].q, bufs[b].k, bufs[b].v, bufs[b].dout), hin):
+                d.copy_(h, non_blocking=True)
+            ready[b].record(copy)
 
-    for _ in range(warmup):
-        step()
+    def run(nsteps):
+        for b in range(2):
+            done[b].record(comp)
+            fetched[b].record(comp)
+        upload(0)
+        for s in range(nsteps):
+            b = s & 1
+            if s + 1 < nsteps:
+                upload(b ^ 1)
+            comp.wait_event(ready[b])
+            comp.wait_event(fetched[b])  # its previous outputs were read back
+            run_step(bufs[b], causal, scale)
+            done[b].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[b])
+                for h, d in zip(hout[b], (bufs[b].dq, bufs[b].dk, bufs[b].dv)):
+                    h.copy_(d, non_blocking=True)
+                fetched[b].record(copy)
+        comp.wait_stream(copy)
+
+    run(warmup)
     barrier(dist_on)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        step()
-    stop.record()
+    start.record(comp)
+    run(steps)
+    stop.record(comp)
     barrier(dist_on)
     ms = max_over_ranks(start.elapsed_time(stop), dist_on) / steps
     h2d = sum(t.numel() * t.element_size() for t in hin)
-    d2h = sum(t.numel() * t.element_size() for t in hout)
+    d2h = sum(t.numel() * t.element_size() for t in hout[0])
     return ms, h2d, d2h
 
 

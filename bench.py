@@ -441,10 +441,10 @@ def main():
     peak = peaks["bf16_tflops_sustained"]
     if bwd_ms >= fwd_ms:
         dom, dom_ms, dom_fl = "fa_bwd (preprocess + main + dQ convert)", bwd_ms, fb
-        traffic = recorded_traffic("fa_bwd_kernel")
+        traffic = recorded_traffic("fa_bwd") if S == WORKLOAD["S"] else None
     else:
         dom, dom_ms, dom_fl = "fa_fwd_kernel", fwd_ms, ff
-        traffic = recorded_traffic("fa_fwd_kernel")
+        traffic = recorded_traffic("fa_fwd_kernel") if S == WORKLOAD["S"] else None
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,

@@ -307,24 +307,39 @@ namespace {
 // fa_bwd and fa_bwd_deterministic; sem == nullptr selects the atomic-order dQ.
 fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const void *dout,
                    const float *lse, float *dq_acc, float *delta, int *sem, void *dq, void *dk,
-                   void *dv, int B, int H, int S, int D, int causal, float scale, void *stream) {
+                   void *dv, int B, int H, int S, int D, int causal, float scale, int pair_mode,
+                   void *stream) {
     const void *ptrs[11] = {q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv};
     for (const void *p : ptrs)
         if (!p || !aligned16(p)) return FA_ERR_INVALID_ARG;
     fa_status st = check_shape(B, H, S, D, scale);
     if (st != FA_OK) return st;
+    if (pair_mode < -1 || pair_mode > 1) return FA_ERR_INVALID_ARG;
+    // CTA pairs: D = 128 with atomic-order dQ only.  Not the default: on
+    // GB300 the single-CTA kernel is faster (the pair's dQ MMA, M = 128 over
+    // two SMs, runs at half the per-SM tensor rate, and the dS exchange adds
+    // latency to the block chain)
+    const bool pair = pair_mode == 1;
+    if (pair && (D != 128 || sem)) return FA_ERR_UNSUPPORTED;
     const DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != FA_OK) return st;
     if ((st = get_encoder()) != FA_OK) return st;
     fa::BwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    // D = 256 streams 64-query blocks and stages dQ as 32 x 32 tiles
-    const unsigned qrows = D == 256 ? 64 : 128, dqrows = D == 256 ? 32 : 128;
+    // D = 256 streams 64-query blocks and stages dQ as 32 x 32 tiles; CTA
+    // pairs stage dQ as 32 x 64 tiles
+    const unsigned qrows = D == 256 ? 64 : 128;
+    const unsigned dqrows = D == 256 ? 32 : (pair ? 64 : 128);
     if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_do, dout, B, S, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, B * H, S, D, dqrows)) != FA_OK) return st;
+    if (pair) {
+        if ((st = make_map_bshd(&a.tm_q64, q, B, S, H, D, 64)) != FA_OK) return st;
+        if ((st = make_map_bshd(&a.tm_do64, dout, B, S, H, D, 64)) != FA_OK) return st;
+    }
+    a.pair = pair ? 1 : 0;
     a.o = o;
     a.dout = dout;
     a.lse = lse;
@@ -356,7 +371,15 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
                  int B, int H, int S, int D, int causal, float scale, void *stream) {
     return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, B, H, S, D,
-                    causal, scale, stream);
+                    causal, scale, -1, stream);
+}
+
+fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                    const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
+                    int B, int H, int S, int D, int causal, float scale, int pair_mode,
+                    void *stream) {
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, B, H, S, D,
+                    causal, scale, pair_mode, stream);
 }
 
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D) {
@@ -371,7 +394,7 @@ fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, cons
                                int D, int causal, float scale, void *stream) {
     if (!dq_sem || !aligned16(dq_sem)) return FA_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, B, H, S, D,
-                    causal, scale, stream);
+                    causal, scale, 0, stream);
 }
 
 fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream) {

@@ -109,31 +109,33 @@ __device__ __forceinline__ int first_block(int j, int causal) { return causal ? 
 
 // 128x128 (x D) with both operands K-major: S^T = K Q^T, dP^T = V dO^T
 template <int D>
+// (descriptors built once per call; a K step adds its byte offset / 16)
 __device__ __forceinline__ void issue_kmajor(uint32_t tD, uint32_t a_saddr, uint32_t b_saddr) {
+    const uint64_t ad = sdesc_sw128(a_saddr, 16, 1024), bd = sdesc_sw128(b_saddr, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
-        mma_ss(tD, sdesc_sw128(a_saddr + off, 16, 1024), sdesc_sw128(b_saddr + off, 16, 1024),
-               BwdCfg<D>::kIdescSS, kk > 0 ? 1u : 0u);
+        const uint32_t off16 = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+        mma_ss(tD, ad + off16, bd + off16, BwdCfg<D>::kIdescSS, kk > 0 ? 1u : 0u);
     }
 }
 
 // acc (+)= A[tmem: 128 keys x 128 queries] * B[smem: 128 queries x D, MN-major]
 template <int D>
 __device__ __forceinline__ void issue_acc(uint32_t tAcc, uint32_t tA, uint32_t b_saddr, bool acc) {
+    const uint64_t bd = sdesc_sw128(b_saddr, kBox, 1024);
 #pragma unroll
     for (int kk = 0; kk < kBlk / 16; ++kk)
-        mma_ts(tAcc, tA + kk * 8, sdesc_sw128(b_saddr + kk * 2048, kBox, 1024),
-               BwdCfg<D>::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+        mma_ts(tAcc, tA + kk * 8, bd + ((kk * 2048) >> 4), BwdCfg<D>::kIdescAcc,
+               (acc || kk > 0) ? 1u : 0u);
 }
 
 // dQ = dS K: A = dS (queries x keys, MN-major: rows = keys), B = K (keys x D, MN-major)
 template <int D>
 __device__ __forceinline__ void issue_dq(uint32_t tD, uint32_t ds_saddr, uint32_t k_saddr) {
+    const uint64_t ad = sdesc_sw128(ds_saddr, kBox, 1024), bd = sdesc_sw128(k_saddr, kBox, 1024);
 #pragma unroll
     for (int kk = 0; kk < kBlk / 16; ++kk)
-        mma_ss(tD, sdesc_sw128(ds_saddr + kk * 2048, kBox, 1024),
-               sdesc_sw128(k_saddr + kk * 2048, kBox, 1024), BwdCfg<D>::kIdescDQ,
+        mma_ss(tD, ad + ((kk * 2048) >> 4), bd + ((kk * 2048) >> 4), BwdCfg<D>::kIdescDQ,
                kk > 0 ? 1u : 0u);
 }
 
@@ -681,6 +683,11 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     fa_bwd_prep<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (a.pair) {
+        if ((e = launch_bwd_main_pair(a, stream)) != cudaSuccess) return e;
+        fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
     auto kern = fa_bwd_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;

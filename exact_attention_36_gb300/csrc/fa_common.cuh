@@ -30,7 +30,9 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [B,S,H,D], same boxes as the forward
-    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 128 x 1 (D = 256: 32 x 32 x 1)
+    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 128 x 1 (D = 256 or
+                                          // CTA pairs: 32 x 32 x 1 / 32 x 64 x 1)
+    CUtensorMap tm_q64, tm_do64;          // CTA pairs: Q and dO with 64-row boxes
     const void *o, *dout;                 // bf16 [B,S,H,D]
     const float *lse;                     // fp32 [B,H,S]
     float *dq_acc;                        // fp32 [B,H,S,D]
@@ -43,6 +45,7 @@ struct BwdArgs {
     float scale_log2;
     int *err_word;
     int num_sms;
+    int pair;                             // 1: D = 128 main kernel on CTA pairs
 };
 
 // Launchers (defined in fa_fwd.cu / fa_bwd.cu).  Return the CUDA error of the
@@ -52,5 +55,8 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream);
 // main backward kernel for D = 256 (fa_bwd_d256.cu); Q/dO tensor maps with
 // 64-row boxes and a dQ-accumulator map with 32 x 32 boxes
 cudaError_t launch_bwd_main_d256(const BwdArgs &a, cudaStream_t stream);
+// main backward kernel for D = 128 on CTA pairs (fa_bwd_pair.cu); Q/dO maps
+// with 128- and 64-row boxes and a dQ-accumulator map with 32 x 64 boxes
+cudaError_t launch_bwd_main_pair(const BwdArgs &a, cudaStream_t stream);
 
 }  // namespace fa

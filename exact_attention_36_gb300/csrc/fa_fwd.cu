@@ -98,23 +98,26 @@ __device__ __forceinline__ bool unit_at(int it, int U, int BH, int P, Unit &out)
 
 // S = Q K^T for one 128x128 tile: both operands K-major (head dim contiguous).
 template <int D>
+// The descriptors are built once per call; a K step only adds its byte offset
+// / 16 to the start-address field (one add per operand), which keeps the single
+// issuing thread ahead of the tensor core.
 __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_saddr, uint32_t k_saddr) {
+    const uint64_t qd = sdesc_sw128(q_saddr, 16, 1024), kd = sdesc_sw128(k_saddr, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
-        mma_ss(tS, sdesc_sw128(q_saddr + off, 16, 1024), sdesc_sw128(k_saddr + off, 16, 1024),
-               FwdCfg<D>::kIdescS, kk > 0 ? 1u : 0u);
+        const uint32_t off16 = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+        mma_ss(tS, qd + off16, kd + off16, FwdCfg<D>::kIdescS, kk > 0 ? 1u : 0u);
     }
 }
 
 // O (+)= P V: P from TMEM, V MN-major (head dim contiguous, keys along K).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_saddr, bool acc) {
+    const uint64_t vd = sdesc_sw128(v_saddr, kBox, 1024);
 #pragma unroll
-    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-        mma_ts(tO, tP + kk * 8, sdesc_sw128(v_saddr + kk * 2048, kBox, 1024),
-               FwdCfg<D>::kIdescPV, (acc || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < kBlockN / 16; ++kk)
+        mma_ts(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), FwdCfg<D>::kIdescPV,
+               (acc || kk > 0) ? 1u : 0u);
 }
 
 template <int D, int POLY_PER8>

@@ -260,7 +260,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle.
+// Shared-memory matrix descriptor, 128-byte swizzle.  The start-address
+// field holds (address & 0x3FFFF) >> 4 of a shared-window address below
+// 256 KB, so the descriptor of the same tile at +off bytes (off a multiple of
+// 16) is desc + (off >> 4): no carry leaves the 14-bit field.
 // Bits: [0,14) start >> 4, [16,30) leading byte offset >> 4, [32,46) stride
 // byte offset >> 4, [46,48) = 1 (descriptor version), [61,64) = 2 (128B
 // swizzle).  Swizzle atoms (8 rows x 128 B) sit on 1024-byte boundaries.
@@ -346,6 +349,89 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef FA_R8
 #undef FA_W8
 #undef FA_RW8
+
+// ----------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on neighbouring SMs.  tcgen05 operations with
+// .cta_group::2 act on both CTAs: Tensor Memory is allocated collectively (one
+// warp of each CTA; both receive the same address), an MMA issued by one
+// thread of rank 0 takes A rows from both CTAs' shared memory or Tensor Memory
+// (M = 256: 128 rows each) and B columns half from each (N/2 each), and its
+// commit can arrive on the same barrier offset in both CTAs.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs; orders earlier memory accesses before later ones
+// cluster-wide.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier anywhere in the cluster (address from mapa_shared),
+// with the default CTA-scope release: measured on GB300, a cluster-scope
+// release costs about 1300 cycles per arrive.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// shared memory anywhere in the cluster; completion (bytes) is counted on the
+// destination CTA's mbarrier `cl_bar` (addresses from mapa_shared).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t cl_dst, const void *src,
+                                                     uint32_t bytes, uint32_t cl_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(cl_dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(cl_bar)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` (same offset) in both CTAs of the pair when every
+// tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
 
 // ----------------------------------------------------------------- math
 

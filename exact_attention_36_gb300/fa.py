@@ -50,6 +50,7 @@ def lib():
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp]
+        L.fa_bwd_ex.argtypes = [vp] * 11 + [i, i, i, i, i, f, i, vp]
         L.fa_bwd_deterministic.argtypes = [vp] * 12 + [i, i, i, i, i, f, vp]
         L.fa_bwd_semaphore_bytes.argtypes = [i, i, i, i]
         L.fa_bwd_semaphore_bytes.restype = ctypes.c_size_t
@@ -59,7 +60,8 @@ def lib():
         L.fa_device_error.argtypes = [ctypes.POINTER(i), i]
         L.fa_exp2_eval.argtypes = [vp, vp, ll, i, vp]
         L.fa_exp2_sweep.argtypes = [f, f, i, vp, vp]
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_deterministic", "fa_last_cuda_error",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_deterministic",
+                     "fa_last_cuda_error",
                      "fa_device_error",
                      "fa_exp2_eval", "fa_exp2_sweep"):
             getattr(L, name).restype = i
@@ -109,13 +111,17 @@ def bwd_workspace_size(B: int, H: int, S: int, D: int) -> int:
 
 
 def bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal: bool, scale: float,
-        stream=None):
-    """fa_bwd on caller-provided tensors (dq, dk, dv written)."""
+        stream=None, pair_mode: int = DEFAULT):
+    """fa_bwd (pair_mode -1) or fa_bwd_ex on caller-provided tensors (dq, dk,
+    dv written).  pair_mode: 0 one CTA per key tile, 1 CTA pairs (D = 128)."""
     B, S, H, D = q.shape
-    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq_acc),
-                      _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), B, H, S, D,
-                      int(bool(causal)), float(scale), _stream(stream))
-    _check("fa_bwd", st)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq_acc),
+            _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), B, H, S, D, int(bool(causal)),
+            float(scale))
+    if pair_mode == DEFAULT:
+        _check("fa_bwd", lib().fa_bwd(*args, _stream(stream)))
+    else:
+        _check("fa_bwd_ex", lib().fa_bwd_ex(*args, int(pair_mode), _stream(stream)))
 
 
 def bwd_deterministic(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, causal: bool,
@@ -155,11 +161,13 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
 
 
 def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
-             stream=None, deterministic: bool = False):
+             stream=None, deterministic: bool = False, pair_mode: int = DEFAULT):
     """Exact attention backward.  Returns (dq, dk, dv), bf16 [B, S, H, D].
 
     deterministic=True sums dQ over key tiles in a fixed order, so repeated
-    calls give bitwise-identical results (dK and dV always are)."""
+    calls give bitwise-identical results (dK and dV always are).
+    pair_mode selects the main kernel: 0 one CTA per key tile, 1 CTA pairs
+    (D = 128 only), -1 the library default."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _check_bshd(name, t, q.shape)
     B, S, H, D = q.shape
@@ -179,7 +187,7 @@ def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
         bwd_deterministic(q, k, v, o, dout, lse, dq_acc, delta, sem, dq, dk, dv, causal, scale,
                           stream)
     else:
-        bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal, scale, stream)
+        bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal, scale, stream, pair_mode)
     return dq, dk, dv
 
 

@@ -115,6 +115,27 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  int B, int H, int S, int D, int causal, float scale, void *stream);
 
 /*
+ * Backward with the choice of main kernel ([nl] Methodologie §3: the 2-CTA
+ * MMA mode splits operand B between two CTAs, and the pair exchanges halves
+ * of the dQ work through distributed shared memory).
+ *   pair_mode : 0  one CTA per 128-key tile (every head dimension);
+ *               1  CTA pairs: two neighbouring SMs own two adjacent key tiles
+ *                  and issue their MMAs together (tcgen05 .cta_group::2);
+ *                  each CTA stages half of every Q/dO operand the MMAs read
+ *                  and reduces only half of the dQ rows.  D = 128 only
+ *                  (other D: FA_ERR_UNSUPPORTED);
+ *              -1  library default (0: on GB300 the pair kernel measures
+ *                  slower, see the kernel's source).
+ * Other arguments, results and errors as fa_bwd; dQ differs from pair_mode 0
+ * only in the order of its fp32 sums.
+ */
+fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                    const void *dout, const float *lse, float *dq_acc, float *delta,
+                    void *dq, void *dk, void *dv,
+                    int B, int H, int S, int D, int causal, float scale, int pair_mode,
+                    void *stream);
+
+/*
  * Deterministic backward ([nl] Methodologie §3 and Belangrijkste Resultaten:
  * a deterministic mode ordered by semaphores): the same results as fa_bwd,
  * except that every element of dQ is summed over the key tiles in a fixed

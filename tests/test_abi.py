@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+    for must in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size",
+                 "fa_status_string",
                  "fa_last_cuda_error", "fa_device_error", "fa_exp2_eval", "fa_exp2_sweep"):
         assert must in names
 
@@ -70,6 +71,14 @@ def test_argument_errors_need_no_device(lib):
     ptrs = [p] * 11
     ptrs[6] = null
     assert lib.fa_bwd(*ptrs, 1, 1, 128, 64, 0, 0.1, null) == fa.FA_ERR_INVALID_ARG
+    # backward main-kernel choice: CTA pairs exist for D = 128 only
+    ok = [p] * 11
+    lib.fa_bwd_ex.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 5 + \
+        [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
+    for mode in (-2, 2):
+        assert lib.fa_bwd_ex(*ok, 1, 1, 128, 128, 0, 0.1, mode, null) == fa.FA_ERR_INVALID_ARG
+    for D in (64, 256):
+        assert lib.fa_bwd_ex(*ok, 1, 1, 128, D, 0, 0.1, 1, null) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_exp2_sweep(1.0, 0.0, 0, p, null) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_exp2_eval(p, p, -1, 0, null) == fa.FA_ERR_INVALID_ARG
 

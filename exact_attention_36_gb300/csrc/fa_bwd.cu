@@ -470,17 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     uint32_t dsw[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
+                        // dS = P o (dP - Delta): the difference in fp32, rounded to
+                        // bf16 and multiplied by the bf16 P, two columns per instruction
                         const float4 d4 = *reinterpret_cast<const float4 *>(dlt + c * 32 + e);
-                        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float ds[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const uint32_t pw = pk[(c * 32 + e + u) >> 1];
-                            const float pv = __uint_as_float(((e + u) & 1) ? (pw & 0xffff0000u) : (pw << 16));
-                            ds[u] = pv * (__uint_as_float(dr[e + u]) - dv4[u]);
-                        }
-                        dsw[e / 2] = pack_bf16x2(ds[0], ds[1]);
-                        dsw[e / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+                        const float2 t0 = sub2(make_float2(__uint_as_float(dr[e]),
+                                                           __uint_as_float(dr[e + 1])),
+                                               make_float2(d4.x, d4.y));
+                        const float2 t1 = sub2(make_float2(__uint_as_float(dr[e + 2]),
+                                                           __uint_as_float(dr[e + 3])),
+                                               make_float2(d4.z, d4.w));
+                        dsw[e / 2] = mul_bf16x2(pk[(c * 32 + e) >> 1], pack_bf16x2(t0.x, t0.y));
+                        dsw[e / 2 + 1] = mul_bf16x2(pk[(c * 32 + e + 2) >> 1], pack_bf16x2(t1.x, t1.y));
                     }
                     tmem_st16(tY + c * 16, dsw);
                     // shared copy for the dQ MMA: queries [32c, 32c+32) of this key row,

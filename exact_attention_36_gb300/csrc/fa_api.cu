@@ -326,10 +326,10 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     if ((st = get_encoder()) != FA_OK) return st;
     fa::BwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    // D = 256 streams 64-query blocks and stages dQ as 32 x 32 tiles; CTA
-    // pairs stage dQ as 32 x 64 tiles
+    // D = 256 streams 64-query blocks; dQ is staged as 32 x 32 tiles (each
+    // drain warp its own), 32 x 64 on CTA pairs
     const unsigned qrows = D == 256 ? 64 : 128;
-    const unsigned dqrows = D == 256 ? 32 : (pair ? 64 : 128);
+    const unsigned dqrows = pair ? 64 : 32;
     if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;

@@ -19,9 +19,14 @@
 // dO_i stream through.  Everything is computed transposed (keys on the 128
 // TMEM lanes), so P^T and dS^T land in Tensor Memory exactly where the dV
 // and dK MMAs want their A operand:
-//   S^T  = K_j Q_i^T      -> X   (fp32, 128 cols)    A=K smem, B=Q smem
-//   dP^T = V_j dO_i^T     -> Y   (fp32, 128 cols)    A=V smem, B=dO smem
-//   P^T (bf16) over X;  dS^T (bf16) over Y and into shared memory
+//   S^T  = K_j Q_i^T - LSE/scale   -> X (fp32, 128 cols)  A=K smem, B=Q smem
+//   dP^T = V_j dO_i^T - Delta      -> Y (fp32, 128 cols)  A=V smem, B=dO smem
+//   P^T = 2^(X scale log2 e) (bf16) over X;  dS^T = P^T o Y (bf16) over Y and
+//   into shared memory
+// The per-query terms -LSE/scale and -Delta enter through one extra K step
+// of those two MMAs: A = ones, B = the value as three bf16 terms (exact sum),
+// written by the producer next to Q_i and dO_i.  The softmax warps then read
+// no per-query statistics from shared memory, whose bandwidth the MMAs need.
 //   dV  += P^T dO_i       (TMEM acc, D cols)         A=X tmem,  B=dO smem
 //   dK  += dS^T Q_i       (TMEM acc, D cols)         A=Y tmem,  B=Q smem
 //   dQ_i = dS K_j  -> Y   (fp32, queries on lanes)   A=dS smem, B=K smem
@@ -30,11 +35,13 @@
 // X once dV(i) was issued, dQ(i) may overwrite Y once dK(i) was issued.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer (K_j/V_j per unit; Q_i + LSE/Delta, dO_i per block)
+//   warp 0      TMA producer (K_j/V_j per unit; Q_i + LSE bias rows, dO_i +
+//               Delta bias rows per block)
 //   warp 1      TMEM allocation + MMA issue (one lane)
 //   warps 2-3   idle
 //   warps 4-7   "softmax": P^T and dS^T for one 128x128 block (lane = key)
-//   warps 8-11  dQ drain (lane = query, fp32 atomic add into the accumulator)
+//   warps 8-11  dQ drain (lane = query; TMA bulk reduce-add into the fp32
+//               accumulator)
 //               and the dK / dV epilogue of each unit
 // Causal units are visited longest first (key tile 0 sees every query
 // block) in a serpentine order over the CTAs, as in the forward.
@@ -60,9 +67,15 @@ struct BwdCfg {
     static constexpr int kOffQ = kOffV + kTile;      // 2 stages
     static constexpr int kOffDO = kOffQ + 2 * kTile;  // 1 stage
     static constexpr int kOffDS = kOffDO + kTile;     // dS: 128 keys x 128 queries bf16
-    static constexpr int kOffRed = kOffDS + 32768;    // dQ staging: 2 x (128 rows x 32 fp32)
-    static constexpr int kOffStat = kOffRed + 32768;  // 2 stages x (128 lse2 + 128 delta) fp32
-    static constexpr int kOffBar = kOffStat + 2 * 1024;
+    static constexpr int kOffRed = kOffDS + 32768;    // dQ staging: 4 warps x 32 x 32 fp32
+    // bias K step of S^T and dP^T (no-swizzle K-major, 128 rows x 16 bf16):
+    // A = (1, 1, 1, 0, ...) on every row; B = three bf16 terms of -LSE/scale
+    // (2 stages, with Q) or of -Delta (1 stage, with dO) per query
+    static constexpr int kBias = 4096;
+    static constexpr int kOffOnes = kOffRed + 16384;
+    static constexpr int kOffLb = kOffOnes + kBias;
+    static constexpr int kOffDb = kOffLb + 2 * kBias;
+    static constexpr int kOffBar = kOffDb + kBias;
     // kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full,
     // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dkdv_empty, drain
     static constexpr int kNumBars = 17;
@@ -107,16 +120,39 @@ __device__ __forceinline__ int first_block(int j, int causal) { return causal ? 
 
 // ---------------------------------------------------------------- MMA helpers
 
-// 128x128 (x D) with both operands K-major: S^T = K Q^T, dP^T = V dO^T
-template <int D>
+// Byte offset of element (row r, k) of a no-swizzle K-major 128 x 16 bf16 tile
+// (core matrices of 8 rows x 16 bytes, K-direction stride 128, row-group 256).
+__host__ __device__ constexpr uint32_t bias_off(int r, int k) {
+    return (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2;
+}
+
+// First 16 bytes of a bias row: v as three bf16 terms hi + mid + lo (each the
+// bf16 rounding of what the previous terms leave; the sum equals v for normal
+// fp32 v) in k = 0, 1, 2; an infinite v goes whole into hi.
+__device__ __forceinline__ uint4 bias_row(float v) {
+    const float hi = __bfloat162float(__float2bfloat16_rn(v));
+    if (!isfinite(v)) return make_uint4(pack_bf16x2(hi, 0.f), 0u, 0u, 0u);
+    const float r1 = v - hi;
+    const float mid = __bfloat162float(__float2bfloat16_rn(r1));
+    const float lo = r1 - mid;
+    return make_uint4(pack_bf16x2(hi, mid), pack_bf16x2(lo, 0.f), 0u, 0u);
+}
+
+// 128x128 (x D) with both operands K-major: S^T = K Q^T, dP^T = V dO^T, plus
+// one bias K step that adds B's per-query value (A's ones times its three
+// terms) to every key row: S^T - LSE/scale, dP^T - Delta.
 // (descriptors built once per call; a K step adds its byte offset / 16)
-__device__ __forceinline__ void issue_kmajor(uint32_t tD, uint32_t a_saddr, uint32_t b_saddr) {
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t tD, uint32_t a_saddr, uint32_t b_saddr,
+                                             uint32_t ones_saddr, uint32_t bias_saddr) {
     const uint64_t ad = sdesc_sw128(a_saddr, 16, 1024), bd = sdesc_sw128(b_saddr, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off16 = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
         mma_ss(tD, ad + off16, bd + off16, BwdCfg<D>::kIdescSS, kk > 0 ? 1u : 0u);
     }
+    mma_ss(tD, sdesc_none(ones_saddr, 128, 256), sdesc_none(bias_saddr, 128, 256),
+           BwdCfg<D>::kIdescSS, 1u);
 }
 
 // acc (+)= A[tmem: 128 keys x 128 queries] * B[smem: 128 queries x D, MN-major]
@@ -162,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     uint64_t *drain = bars + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
-    float *stat = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // [stage][lse2 128 | delta 128]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -176,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
         for (int s2 = 0; s2 < 2; ++s2) {
-            mbar_init(&q_full[s2], 2);  // TMA (expect_tx) + LSE/Delta written
+            mbar_init(&q_full[s2], 2);  // TMA (expect_tx) + LSE bias rows written
             mbar_init(&q_empty[s2], 1);
         }
-        mbar_init(do_full, 1);
+        mbar_init(do_full, 2);  // TMA (expect_tx) + Delta bias rows written
         mbar_init(do_empty, 1);
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
@@ -197,6 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         tmem_alloc(tmem_holder, Cfg::kTmemCols);
         tmem_relinquish();
     }
+    // bias tiles: zero everywhere (the MMA reads all 16 K columns), ones in
+    // k = 0, 1, 2 of the A tile
+    for (int t = threadIdx.x; t < 4 * Cfg::kBias / 16; t += kThreads)
+        reinterpret_cast<uint4 *>(smem + Cfg::kOffOnes)[t] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (threadIdx.x < 128)
+        *reinterpret_cast<uint4 *>(smem + Cfg::kOffOnes + bias_off(threadIdx.x, 0)) =
+            make_uint4(pack_bf16x2(1.f, 1.f), pack_bf16x2(1.f, 0.f), 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&args.tm_q);
         tma_prefetch_desc(&args.tm_k);
@@ -215,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 1};
         uint32_t nunit = 0, nblk = 0;  // units / blocks issued so far
         bool ok = true;
-        const float log2e = 1.4426950408889634f;
+        const float inv_scale = 1.f / args.scale;
         for (int it = 0; ok; ++it) {
             BUnit un;
             if (!bunit_at(it, U, BH, un)) break;
@@ -239,41 +283,53 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             ++nunit;
             for (int i = i0; i < nT && ok; ++i, ++nblk) {
                 const int st = nblk & 1;
-                // Q_i (+ LSE and Delta of its rows) into stage st
+                // this block's -LSE/scale and -Delta per query, loaded before the
+                // waits so their latency overlaps them (-inf / 0 past S: P = 0)
+                const size_t rbase = static_cast<size_t>(un.bh) * S;
+                float lv[4], dv[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int q = i * kBlk + r * 32 + lane;
+                    lv[r] = q < S ? -args.lse[rbase + q] * inv_scale : -INFINITY;
+                    dv[r] = q < S ? -args.delta[rbase + q] : 0.f;
+                }
+                // Q_i into stage st, then the bias rows of S^T
                 w.code = kErrBwdWait + 2;
                 ok = mbar_wait(&q_empty[st], ((nblk >> 1) & 1) ^ 1, w);
                 ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
                 if (!ok) break;
                 if (lane == 0) {
-                    // the tile first, so its latency overlaps the LSE/Delta loads
                     mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_4d(smem + Cfg::kOffQ + st * Cfg::kTile + c * kBox, &args.tm_q,
                                     &q_full[st], 64 * c, h, i * kBlk, b);
                 }
-                float *sl = stat + st * 256;
-                const size_t rbase = static_cast<size_t>(un.bh) * S;
+                uint8_t *lb = smem + Cfg::kOffLb + st * Cfg::kBias;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int qr = r * 32 + lane;
-                    const int q = i * kBlk + qr;
-                    const bool in = q < S;
-                    sl[qr] = in ? args.lse[rbase + q] * log2e : INFINITY;
-                    sl[128 + qr] = in ? args.delta[rbase + q] : 0.f;
-                }
+                for (int r = 0; r < 4; ++r)
+                    *reinterpret_cast<uint4 *>(lb + bias_off(r * 32 + lane, 0)) = bias_row(lv[r]);
+                fence_proxy_async_smem();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[st]);
+                // dO_i (single stage: the previous block's dV MMA, and so its
+                // dP^T, has finished), then the bias rows of dP^T
+                w.code = kErrBwdWait + 3;
+                ok = mbar_wait(do_empty, (nblk & 1) ^ 1, w);
+                ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
+                if (!ok) break;
                 if (lane == 0) {
-                    mbar_arrive(&q_full[st]);
-                    // dO_i (single stage)
-                    w.code = kErrBwdWait + 3;
-                    ok = mbar_wait(do_empty, (nblk & 1) ^ 1, w);
-                    if (ok) {
-                        mbar_arrive_expect_tx(do_full, Cfg::kTile);
-                        for (int c = 0; c < Cfg::kBoxes; ++c)
-                            tma_load_4d(smem + Cfg::kOffDO + c * kBox, &args.tm_do, do_full,
-                                        64 * c, h, i * kBlk, b);
-                    }
+                    mbar_arrive_expect_tx(do_full, Cfg::kTile);
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_4d(smem + Cfg::kOffDO + c * kBox, &args.tm_do, do_full,
+                                    64 * c, h, i * kBlk, b);
                 }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    *reinterpret_cast<uint4 *>(smem + Cfg::kOffDb + bias_off(r * 32 + lane, 0)) =
+                        bias_row(dv[r]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(do_full);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             }
         }
@@ -293,6 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             const uint32_t tdV = tmem + Cfg::kTdV, tdK = tmem + Cfg::kTdK;
             const uint32_t aK = sbase + Cfg::kOffK, aV = sbase + Cfg::kOffV;
             const uint32_t aDO = sbase + Cfg::kOffDO, aDS = sbase + Cfg::kOffDS;
+            const uint32_t aOnes = sbase + Cfg::kOffOnes, aLb = sbase + Cfg::kOffLb;
+            const uint32_t aDb = sbase + Cfg::kOffDb;
             uint32_t nunit = 0, nblk = 0;
             uint32_t ph_p = 0, ph_ds = 0, ph_dqe = 0;
             bool ok = true;
@@ -315,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     FA_WAIT(&q_full[st], (nblk >> 1) & 1, 11);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_kmajor<D>(tX, aK, sbase + Cfg::kOffQ + st * Cfg::kTile);
+                    issue_kmajor<D>(tX, aK, sbase + Cfg::kOffQ + st * Cfg::kTile, aOnes,
+                                    aLb + st * Cfg::kBias);
                     mma_commit(s_full);
                     if (nblk > 0) {
                         FA_WAIT(dq_empty, ph_dqe, 12);
@@ -325,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     FA_WAIT(do_full, nblk & 1, 13);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_kmajor<D>(tY, aV, aDO);
+                    issue_kmajor<D>(tY, aV, aDO, aOnes, aDb);
                     mma_commit(dp_full);
                 }
                 for (int i = i0; i < nT; ++i, ++nblk) {
@@ -347,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         FA_WAIT(&q_full[st2], ((nblk + 1) >> 1) & 1, 16);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_kmajor<D>(tX, aK, sbase + Cfg::kOffQ + st2 * Cfg::kTile);
+                        issue_kmajor<D>(tX, aK, sbase + Cfg::kOffQ + st2 * Cfg::kTile, aOnes,
+                                        aLb + st2 * Cfg::kBias);
                         mma_commit(s_full);
                     }
                     FA_WAIT(ds_ready, ph_ds, 17);
@@ -365,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         FA_WAIT(do_full, (nblk + 1) & 1, 19);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_kmajor<D>(tY, aV, aDO);
+                        issue_kmajor<D>(tY, aV, aDO, aOnes, aDb);
                         mma_commit(dp_full);
                     } else {
                         mma_commit(dkdv_full);
@@ -398,14 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             const int i0 = first_block(un.j, args.causal);
             const int key = un.j * kBlk + kr;
             for (int i = i0; i < nT; ++i, ++n) {
-                const int st = n & 1;
-                w.code = kErrBwdWait + 30;
-                if (!mbar_wait(&q_full[st], (n >> 1) & 1, w)) { ok = false; break; }
                 w.code = kErrBwdWait + 31;
                 if (!mbar_wait(s_full, n & 1, w)) { ok = false; break; }
                 tc_fence_after();
-                const float *lse2 = stat + st * 256;
-                const float *dlt = lse2 + 128;
                 uint32_t pk[64];
                 {
                     uint32_t sr[4][32];
@@ -413,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     for (int c = 0; c < 4; ++c) tmem_ld32(tX + c * 32, sr[c]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-                    // visible: key < S and (non-causal or query >= key); rows
-                    // past S carry lse2 = +inf, which gives P = 0
-                    // masking only where a block can hold invisible pairs: the
-                    // causal diagonal block and a key tile reaching past S
-                    // (queries past S carry lse2 = +inf, which gives P = 0)
+                    // X holds S^T - LSE/scale (the bias K step), so P = 2^(X c2).
+                    // Visible: key < S and (non-causal or query >= key); masking
+                    // only where a block can hold invisible pairs: the causal
+                    // diagonal block and a key tile reaching past S (queries past
+                    // S carry a bias of -inf, which gives P = 0)
                     if ((args.causal && i == un.j) || (un.j + 1) * kBlk > S) {
                         const int lim = (args.causal && i == un.j) ? kr : -1;  // col < lim hidden
                         const bool key_ok = key < S;
@@ -431,14 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c * 32 + e);
-                            const float p0 = ex2_mufu(fmaf(__uint_as_float(sr[c][e]), c2, -l4.x));
-                            const float p1 = ex2_mufu(fmaf(__uint_as_float(sr[c][e + 1]), c2, -l4.y));
-                            const float p2 = ex2_mufu(fmaf(__uint_as_float(sr[c][e + 2]), c2, -l4.z));
-                            const float p3 = ex2_mufu(fmaf(__uint_as_float(sr[c][e + 3]), c2, -l4.w));
-                            pk[(c * 32 + e) / 2] = pack_bf16x2(p0, p1);
-                            pk[(c * 32 + e) / 2 + 1] = pack_bf16x2(p2, p3);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 x = mul2(make_float2(__uint_as_float(sr[c][e]),
+                                                              __uint_as_float(sr[c][e + 1])),
+                                                  make_float2(c2, c2));
+                            pk[(c * 32 + e) / 2] = pack_bf16x2(ex2_mufu(x.x), ex2_mufu(x.y));
                         }
                     }
                 }
@@ -448,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(p_ready);
-                // ---- dS^T = P^T o (dP^T - Delta)
+                // ---- dS^T = P^T o (dP^T - Delta); Y holds dP^T - Delta (bias K step)
                 w.code = kErrBwdWait + 32;
                 if (!mbar_wait(dp_full, n & 1, w)) { ok = false; break; }
                 if (n > 0) {
@@ -469,19 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     const uint32_t (&dr)[32] = drr[c - c2i];
                     uint32_t dsw[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        // dS = P o (dP - Delta): the difference in fp32, rounded to
-                        // bf16 and multiplied by the bf16 P, two columns per instruction
-                        const float4 d4 = *reinterpret_cast<const float4 *>(dlt + c * 32 + e);
-                        const float2 t0 = sub2(make_float2(__uint_as_float(dr[e]),
-                                                           __uint_as_float(dr[e + 1])),
-                                               make_float2(d4.x, d4.y));
-                        const float2 t1 = sub2(make_float2(__uint_as_float(dr[e + 2]),
-                                                           __uint_as_float(dr[e + 3])),
-                                               make_float2(d4.z, d4.w));
-                        dsw[e / 2] = mul_bf16x2(pk[(c * 32 + e) >> 1], pack_bf16x2(t0.x, t0.y));
-                        dsw[e / 2 + 1] = mul_bf16x2(pk[(c * 32 + e + 2) >> 1], pack_bf16x2(t1.x, t1.y));
-                    }
+                    for (int e = 0; e < 32; e += 2)
+                        // dS = P o (dP - Delta): the fp32 difference rounded to bf16,
+                        // times the bf16 P, two columns per instruction
+                        dsw[e / 2] = mul_bf16x2(pk[(c * 32 + e) >> 1],
+                                                pack_bf16x2(__uint_as_float(dr[e]),
+                                                            __uint_as_float(dr[e + 1])));
                     tmem_st16(tY + c * 16, dsw);
                     // shared copy for the dQ MMA: queries [32c, 32c+32) of this key row,
                     // 128B-swizzled, two 64-query blocks of 16 KB
@@ -502,15 +547,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-        // dQ_i is staged 32 columns at a time in 128B-swizzled shared memory
-        // and added into the fp32 accumulator by TMA bulk reductions, which
-        // keeps the atomics off the load/store pipe the softmax warps use.
+        // dQ_i is staged 32 x 32 at a time in 128B-swizzled shared memory (one
+        // 4 KB tile per warp) and added into the fp32 accumulator by TMA bulk
+        // reductions, which keeps the atomics off the load/store pipe the
+        // softmax warps use.
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // TMEM lane: query (dQ) or key (dK, dV)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const bool leader = (threadIdx.x == 256);
+        uint8_t *stage = smem + Cfg::kOffRed + quarter * 4096;
+        uint8_t *stage_row = stage + lane * 128;
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 40};
-        uint32_t n = 0, nunit = 0, nred = 0;
+        uint32_t n = 0, nunit = 0;
         bool ok = true;
         for (int it = 0; ok; ++it) {
             BUnit un;
@@ -532,45 +580,50 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&acc[c * 32]));
                 tc_fence_before();
                 mbar_arrive(dq_empty);
+                // deterministic mode: key tile j adds its share of dQ block i only
+                // after tiles 0 .. j-1 have (they are the only tiles before it
+                // that see block i), so every sum runs in key order.  A tile only
+                // ever waits on a smaller unit index (an earlier or concurrent
+                // unit), so the waits cannot form a cycle.
+                int *sem = args.dq_sem ? args.dq_sem + static_cast<size_t>(un.bh) * nSem +
+                                             (i * kBlk) / 64
+                                       : nullptr;
+                bool go = true;
+                if (sem) {
+                    if (lane == 0) {
+                        w.code = kErrBwdWait + 42;
+                        go = counter_wait_geq(sem, un.j, w);
+                        fence_proxy_async_global();
+                    }
+                    go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+                }
+                // each warp stages its 32 query rows, 32 columns at a time, and
+                // reduces them on its own (no wait on the other drain warps)
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c, ++nred) {
-                    uint8_t *buf = smem + Cfg::kOffRed + (nred & 1) * 16384;
-                    if (leader) bulk_wait_read<1>();  // the reduction that last used buf has read it
-                    named_bar_sync(1, 128);
-                    uint8_t *row = buf + r * 128;
+                for (int c = 0; c < D / 32; ++c) {
+                    if (lane == 0) bulk_wait_read<0>();  // the previous reduction has read buf
+                    __syncwarp();
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<uint4 *>(row + ((k ^ (r & 7)) << 4)) =
+                        *reinterpret_cast<uint4 *>(stage_row + ((k ^ (lane & 7)) << 4)) =
                             make_uint4(acc[c * 32 + 4 * k], acc[c * 32 + 4 * k + 1],
                                        acc[c * 32 + 4 * k + 2], acc[c * 32 + 4 * k + 3]);
                     fence_proxy_async_smem();
-                    named_bar_sync(1, 128);
-                    if (leader) {
-                        // deterministic mode: key tile j adds its share of dQ block i
-                        // only after tiles 0 .. j-1 have (they are the only tiles
-                        // before it that see block i), so every sum runs in key order.
-                        // A tile only ever waits on a smaller unit index (an earlier
-                        // or concurrent unit), so the waits cannot form a cycle.
-                        int *sem = args.dq_sem ? args.dq_sem + static_cast<size_t>(un.bh) * nSem +
-                                                     (i * kBlk) / 64
-                                               : nullptr;
-                        bool go = true;
-                        if (sem && c == 0) {
-                            w.code = kErrBwdWait + 42;
-                            go = counter_wait_geq(sem, un.j, w);
-                            fence_proxy_async_global();
-                        }
-                        if (go && !*abort_flag) {
-                            tma_reduce_add_3d(&args.tm_dqacc, buf, 32 * c, i * kBlk, un.bh);
-                            bulk_commit();
-                        }
-                        if (sem && c == D / 32 - 1) {
-                            bulk_wait<0>();  // this block's reductions are done in L2
-                            fence_proxy_async_global();
-                            __threadfence();
-                            red_release_gpu_add(sem, 1);
-                        }
+                    __syncwarp();
+                    if (lane == 0 && go && !*abort_flag) {
+                        tma_reduce_add_3d(&args.tm_dqacc, stage, 32 * c, i * kBlk + quarter * 32,
+                                          un.bh);
+                        bulk_commit();
                     }
+                }
+                if (sem) {
+                    if (lane == 0) {
+                        bulk_wait<0>();  // this warp's reductions are done in L2
+                        fence_proxy_async_global();
+                        __threadfence();
+                    }
+                    named_bar_sync(1, 128);  // and the other three warps'
+                    if (leader) red_release_gpu_add(sem, 1);
                 }
             }
             if (!ok) break;

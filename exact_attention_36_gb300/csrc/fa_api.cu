@@ -156,6 +156,7 @@ __device__ __forceinline__ float exp2_variant(float x, int variant) {
     if (variant == 0) return fa::exp2_poly<3>(x);
     if (variant == 1) return fa::exp2_poly_full<3>(x);
     if (variant == 3) return fa::exp2_poly3_x2(make_float2(x, -x)).x;
+    if (variant == 4) return fa::exp2_poly_full<5>(x);
     return fa::ex2_mufu(x);
 }
 
@@ -398,7 +399,7 @@ fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, cons
 }
 
 fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream) {
-    if (!x || !y || n < 0 || variant < 0 || variant > 3) return FA_ERR_INVALID_ARG;
+    if (!x || !y || n < 0 || variant < 0 || variant > 4) return FA_ERR_INVALID_ARG;
     if (n == 0) return FA_OK;
     const DeviceInfo *d = nullptr;
     fa_status st = device_info(&d);
@@ -412,7 +413,7 @@ fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void 
 
 fa_status fa_exp2_sweep(float lo, float hi, int variant, double *out, void *stream) {
     if (!out || !(std::isfinite(lo) && std::isfinite(hi)) || lo > hi || variant < 0 ||
-        variant > 3)
+        variant > 4)
         return FA_ERR_INVALID_ARG;
     const DeviceInfo *d = nullptr;
     fa_status st = device_info(&d);

@@ -205,7 +205,8 @@ def device_error(clear: bool = True) -> int:
 
 def exp2_eval(x: torch.Tensor, variant: int, stream=None) -> torch.Tensor:
     """Approximate 2^x on the device (variant 0 kernel polynomial, 1 full-range
-    polynomial, 2 MUFU, 3 the kernel polynomial in two-lane form)."""
+    polynomial, 2 MUFU, 3 the kernel polynomial in two-lane form, 4 the
+    degree-5 full-range polynomial)."""
     if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
         raise ValueError("x: expected a contiguous CUDA fp32 tensor")
     y = torch.empty_like(x)

@@ -200,7 +200,9 @@ fa_status fa_device_error(int *code, int clear);
  *   variant 1 = the same polynomial with exact subnormal scaling,
  *   variant 2 = hardware MUFU ex2.approx (flush-to-zero),
  *   variant 3 = the kernel polynomial in its two-lane (f32x2) form, as the
- *               softmax evaluates it (same range and clamp as variant 0).
+ *               softmax evaluates it (same range and clamp as variant 0),
+ *   variant 4 = the degree-5 polynomial ([nl] Methodologie §2: degree 3 or
+ *               5) with exact subnormal scaling, like variant 1.
  * fa_exp2_sweep: every fp32 x with lo <= x <= hi (lo, hi finite, lo <= hi)
  *   is evaluated with `variant` and compared to 2^x in double precision;
  *   the largest relative error |y - 2^x| / max(2^x, 2^-126) and its

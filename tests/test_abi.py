@@ -81,6 +81,7 @@ def test_argument_errors_need_no_device(lib):
         assert lib.fa_bwd_ex(*ok, 1, 1, 128, D, 0, 0.1, 1, null) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_exp2_sweep(1.0, 0.0, 0, p, null) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_exp2_eval(p, p, -1, 0, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_exp2_eval(p, p, 16, 5, null) == fa.FA_ERR_INVALID_ARG
 
 
 def test_workspace_size(lib):

@@ -47,12 +47,20 @@ def test_kernel_polynomial_clamps_below_minus125():
     assert (y > 0).all() and (y <= 2.0 ** -124).all()
 
 
+def test_degree5_polynomial_exhaustive_minus127_to_0():
+    # the pages allow degree 3 or 5; degree 5 is the tighter one (fit ~1.6e-7)
+    err, x = fa.exp2_sweep(-127.0, 0.0, variant=4)
+    assert err <= GATE, (err, x)
+    assert err <= 1e-6
+
+
 def test_mufu_reference_range():
     err, x = fa.exp2_sweep(-126.0, 16.0, variant=2)
     assert err <= 2.0 ** -20, (err, x)
 
 
-@pytest.mark.parametrize("variant,lo,hi", [(1, -127.0, 0.0), (0, -125.0, 16.0), (2, -126.0, 16.0)])
+@pytest.mark.parametrize("variant,lo,hi", [(1, -127.0, 0.0), (0, -125.0, 16.0), (2, -126.0, 16.0),
+                                            (4, -127.0, 0.0)])
 def test_sampled_against_oracle_exp2(variant, lo, hi):
     g = torch.Generator().manual_seed(variant)
     x = lo + (hi - lo) * torch.rand(1 << 20, generator=g, dtype=torch.float64)

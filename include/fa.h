@@ -126,8 +126,8 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
  *                  (other D: FA_ERR_UNSUPPORTED);
  *              -1  library default (0: on GB300 the pair kernel measures
  *                  slower, see the kernel's source).
- * Other arguments, results and errors as fa_bwd; dQ differs from pair_mode 0
- * only in the order of its fp32 sums.
+ * Other arguments, results and errors as fa_bwd; the results agree with
+ * pair_mode 0 to rounding (fp32 operations in a different order).
  */
 fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
                     const void *dout, const float *lse, float *dq_acc, float *delta,

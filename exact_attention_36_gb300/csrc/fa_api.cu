@@ -250,14 +250,21 @@ fa_status fa_device_error(int *code, int clear) {
     return v ? FA_ERR_TIMEOUT : FA_OK;
 }
 
-fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                    int H, int S, int D, int causal, float scale, float rescale_threshold,
-                    int poly_exp2_groups, void *stream) {
+}  // extern "C"
+
+namespace {
+// fa_fwd_ex and fa_fwd_varlen.  cu == nullptr: fixed length, [B, S, H, D];
+// else packed: B sequences in [T, H, D], S = the longest.
+fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu,
+                   int B, int H, int S, int T, int D, int causal, float scale,
+                   float rescale_threshold, int poly_exp2_groups, void *stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
-    fa_status st = check_shape(B, H, S, D, scale);
+    fa_status st = cu ? check_shape(1, H, T, D, scale) : check_shape(B, H, S, D, scale);
     if (st != FA_OK) return st;
+    if (cu && (B < 1 || S < 1 || S > T || (reinterpret_cast<uintptr_t>(cu) & 3u)))
+        return FA_ERR_INVALID_ARG;
     if (rescale_threshold < 0.f) rescale_threshold = kDefaultRescaleThreshold;
     if (!(rescale_threshold <= 16.f)) return FA_ERR_INVALID_ARG;
     if (poly_exp2_groups < 0) poly_exp2_groups = kDefaultPolyGroups;
@@ -269,9 +276,10 @@ fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float 
     if ((st = get_encoder()) != FA_OK) return st;
     fa::FwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
+    const int mb = cu ? 1 : B, ms = cu ? T : S;  // the tensors' [B, S] as the maps see them
+    if ((st = make_map_bshd(&a.tm_q, q, mb, ms, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_k, k, mb, ms, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_v, v, mb, ms, H, D)) != FA_OK) return st;
     a.o = o;
     a.lse = lse;
     a.B = B;
@@ -284,9 +292,29 @@ fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float 
     a.poly_groups = poly_exp2_groups;
     a.err_word = d->err_word;
     a.num_sms = d->num_sms;
+    a.cu_seqlens = cu;
+    a.T = cu ? T : B * S;
     cudaError_t e = fa::launch_fwd(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int H, int S, int D, int causal, float scale, float rescale_threshold,
+                    int poly_exp2_groups, void *stream) {
+    return fwd_impl(q, k, v, o, lse, nullptr, B, H, S, 0, D, causal, scale, rescale_threshold,
+                    poly_exp2_groups, stream);
+}
+
+fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                        const int *cu_seqlens, int B, int max_seqlen, int total, int H, int D,
+                        int causal, float scale, void *stream) {
+    if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, lse, cu_seqlens, B, H, max_seqlen, total, D, causal, scale, -1.f,
+                    -1, stream);
 }
 
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,

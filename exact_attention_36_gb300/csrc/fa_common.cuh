@@ -13,6 +13,8 @@ enum DeviceError : int {
     kErrNone = 0,
     kErrFwdWait = 0x100,  // + site
     kErrBwdWait = 0x200,  // + site
+    kErrSeqlens = 0x300,  // packed batches: cu_seqlens not non-decreasing within
+                          // [0, T] or a sequence longer than max_seqlen
 };
 
 struct FwdArgs {
@@ -26,6 +28,8 @@ struct FwdArgs {
     int poly_groups;          // columns of every 8 whose exp2 uses the FMA polynomial
     int *err_word;            // device error word
     int num_sms;
+    const int *cu_seqlens;    // packed variable-length batch: B+1 offsets, else null
+    int T;                    // packed: total tokens (S is then the longest sequence)
 };
 
 struct BwdArgs {
@@ -46,7 +50,49 @@ struct BwdArgs {
     int *err_word;
     int num_sms;
     int pair;                             // 1: D = 128 main kernel on CTA pairs
+    const int *cu_seqlens;                // packed variable-length batch, else null
+    int T;                                // packed: total tokens (S = longest sequence)
 };
+
+// Rows of batch entry b.  Fixed length: rows [0, S) of entry b, read through
+// [B, S, H, D] tensor maps (TMA row coordinate = row, batch coordinate b).
+// Packed variable length (cu != null): rows [cu[b], cu[b+1]) of [T, H, D]
+// tensors, read through [1, T, H, D] maps; per-query statistics, Delta and the
+// dQ accumulator are then [H, T] (and [H, T, D]).  An entry whose offsets are
+// out of order, past T or longer than S is marked bad (len 0).
+struct SeqSpan {
+    int tok0;   // token index of row 0 (b*S for fixed length)
+    int len;    // rows
+    int trow0;  // TMA row coordinate of row 0
+    int tb;     // TMA batch coordinate
+    bool ok;
+};
+
+__device__ __forceinline__ SeqSpan seq_span(const int *cu, int T, int S, int b) {
+    SeqSpan s;
+    if (cu) {
+        const int a0 = __ldg(cu + b), a1 = __ldg(cu + b + 1);
+        s.ok = 0 <= a0 && a0 <= a1 && a1 <= T && a1 - a0 <= S;
+        s.tok0 = a0;
+        s.len = s.ok ? a1 - a0 : 0;
+        s.trow0 = a0;
+        s.tb = 0;
+    } else {
+        s.ok = true;
+        s.tok0 = b * S;
+        s.len = S;
+        s.trow0 = 0;
+        s.tb = b;
+    }
+    return s;
+}
+
+// Index of (b, h, row) in the per-query arrays: [B, H, S], or [H, T] packed.
+__device__ __forceinline__ size_t stat_index(const int *cu, int T, int S, int H, int b, int h,
+                                             const SeqSpan &sp, int row) {
+    return cu ? static_cast<size_t>(h) * T + sp.tok0 + row
+              : (static_cast<size_t>(b) * H + h) * S + row;
+}
 
 // Launchers (defined in fa_fwd.cu / fa_bwd.cu).  Return the CUDA error of the
 // launch (cudaSuccess when enqueued).

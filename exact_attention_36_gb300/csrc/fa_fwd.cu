@@ -142,9 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int lane = threadIdx.x & 31;
     const int H = args.H, S = args.S;
     const int BH = args.B * H;
-    const int P = (S + Cfg::kRows - 1) / Cfg::kRows;
+    const int P = (S + Cfg::kRows - 1) / Cfg::kRows;  // S: the longest sequence if packed
     const int U = BH * P;
-    const int nKV = (S + kBlockN - 1) / kBlockN;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -177,14 +176,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t tmem = *tmem_holder;
     const uint32_t smem_base = smem_u32(smem);
 
-    // key tiles visited by query tile 0 / 1 of unit p
+    // key tiles visited by query tile 0 / 1 of unit p of a sequence of len rows
     // (with a single query tile, n1 = n0)
-    auto tiles_for = [&](int p, int &n0, int &n1) {
+    auto tiles_for = [&](int p, int len, int &n0, int &n1) {
         if (args.causal) {
-            n0 = min(p * Cfg::kRows + kBlockM - 1, S - 1) / kBlockN + 1;
-            n1 = min(p * Cfg::kRows + Cfg::kNQ * kBlockM - 1, S - 1) / kBlockN + 1;
+            n0 = min(p * Cfg::kRows + kBlockM - 1, len - 1) / kBlockN + 1;
+            n1 = min(p * Cfg::kRows + Cfg::kNQ * kBlockM - 1, len - 1) / kBlockN + 1;
         } else {
-            n0 = n1 = nKV;
+            n0 = n1 = (len + kBlockN - 1) / kBlockN;
         }
     };
 
@@ -199,8 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 if (!unit_at(it, U, BH, P, un)) break;
                 if (un.p < 0) continue;
                 const int b = un.bh / H, h = un.bh % H;
+                const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
+                if (!sp.ok && un.p == 0 && h == 0) atomicCAS(args.err_word, 0, kErrSeqlens);
+                if (un.p * Cfg::kRows >= sp.len) continue;  // past this sequence's end
                 int n0, n1;
-                tiles_for(un.p, n0, n1);
+                tiles_for(un.p, sp.len, n0, n1);
                 w.code = kErrFwdWait + 1;
                 if (!mbar_wait(q_empty, (qi & 1) ^ 1, w)) { ok = false; break; }
                 ++qi;
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 for (int t = 0; t < Cfg::kNQ; ++t)
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_4d(smem + t * Cfg::kTileBytes + c * kBox, &args.tm_q, q_full,
-                                    64 * c, h, un.p * Cfg::kRows + t * kBlockM, b);
+                                    64 * c, h, sp.trow0 + un.p * Cfg::kRows + t * kBlockM, sp.tb);
                 for (int j = 0; j < n1 && ok; ++j) {
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t slot = ring % Cfg::kStages;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         const CUtensorMap *map = which ? &args.tm_v : &args.tm_k;
                         for (int c = 0; c < Cfg::kBoxes; ++c)
                             tma_load_4d(dst + c * kBox, map, &kv_full[slot], 64 * c, h,
-                                        j * kBlockN, b);
+                                        sp.trow0 + j * kBlockN, sp.tb);
                         ++ring;
                     }
                 }
@@ -250,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 Unit un;
                 if (!unit_at(it, U, BH, P, un)) break;
                 if (un.p < 0) continue;
+                const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
+                if (un.p * Cfg::kRows >= sp.len) continue;
                 int n0, n1;
-                tiles_for(un.p, n0, n1);
+                tiles_for(un.p, sp.len, n0, n1);
                 w.code = kErrFwdWait + 10;
                 if (!mbar_wait(q_full, qi & 1, w)) { ok = false; break; }
                 ++qi;
@@ -346,8 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             if (!unit_at(it, U, BH, P, un)) break;
             if (un.p < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
+            if (un.p * Cfg::kRows >= sp.len) continue;
+            const int len = sp.len;
             int n0, n1;
-            tiles_for(un.p, n0, n1);
+            tiles_for(un.p, len, n0, n1);
             const int n = t ? n1 : n0;
             const int row = un.p * Cfg::kRows + t * kBlockM + r_in_tile;
             float m_used = -INFINITY;  // reference maximum, log2 units of scaled scores
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
                 if (j == n - 1) {
                     // last tile of the row: keys past S and, if causal, past the row
-                    const int lim = (args.causal ? min(row, S - 1) : S - 1) - j * kBlockN;
+                    const int lim = (args.causal ? min(row, len - 1) : len - 1) - j * kBlockN;
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -444,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             tc_fence_after();
             const float inv_l = 1.f / l;
             uint16_t *orow = reinterpret_cast<uint16_t *>(args.o) +
-                             ((static_cast<size_t>(b) * S + row) * H + h) * D;
+                             ((static_cast<size_t>(sp.tok0) + row) * H + h) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
                                         __uint_as_float(orr[2 * e + 1]) * inv_l);
-                if (row < S) {
+                if (row < len) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
@@ -463,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                                              pk[4 * v4 + 3]);
                 }
             }
-            if (row < S)
-                args.lse[(static_cast<size_t>(b) * H + h) * S + row] =
+            if (row < len)
+                args.lse[stat_index(args.cu_seqlens, args.T, S, H, b, h, sp, row)] =
                     (m_used + log2f(l)) * 0.69314718055994531f;
         }
     }

@@ -47,6 +47,7 @@ def lib():
         vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]
+        L.fa_fwd_varlen.argtypes = [vp] * 6 + [i, i, i, i, i, i, f, vp]
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp]
@@ -60,7 +61,8 @@ def lib():
         L.fa_device_error.argtypes = [ctypes.POINTER(i), i]
         L.fa_exp2_eval.argtypes = [vp, vp, ll, i, vp]
         L.fa_exp2_sweep.argtypes = [f, f, i, vp, vp]
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_deterministic",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_bwd", "fa_bwd_ex",
+                     "fa_bwd_deterministic",
                      "fa_last_cuda_error",
                      "fa_device_error",
                      "fa_exp2_eval", "fa_exp2_sweep"):
@@ -104,6 +106,18 @@ def fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None,
                          int(bool(causal)), float(scale), float(rescale_threshold),
                          int(poly_exp2_groups), _stream(stream))
     _check("fa_fwd", st)
+
+
+def fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, scale: float,
+               stream=None):
+    """fa_fwd_varlen on caller-provided tensors: q, k, v, o bf16 [T, H, D],
+    lse fp32 [H, T], cu_seqlens int32 [B+1] on the device."""
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    _check("fa_fwd_varlen", lib().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                _ptr(cu_seqlens), B, int(max_seqlen), T, H, D,
+                                                int(bool(causal)), float(scale),
+                                                _stream(stream)))
 
 
 def bwd_workspace_size(B: int, H: int, S: int, D: int) -> int:
@@ -189,6 +203,39 @@ def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
     else:
         bwd(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, causal, scale, stream, pair_mode)
     return dq, dk, dv
+
+
+def _check_packed(name, t, shape=None):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA bf16 tensor [T, H, D]")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+
+
+def _check_cu(cu_seqlens, device):
+    if (not cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1
+            or cu_seqlens.numel() < 2 or not cu_seqlens.is_contiguous()
+            or cu_seqlens.device != device):
+        raise ValueError("cu_seqlens: expected a contiguous CUDA int32 tensor [B+1]")
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
+                   scale: float | None = None, stream=None):
+    """Exact attention over a packed batch: sequence b is tokens
+    [cu_seqlens[b], cu_seqlens[b+1]) of q, k, v (CUDA bf16 [T, H, D]).
+
+    Returns (o bf16 [T, H, D], lse fp32 [H, T])."""
+    _check_packed("q", q)
+    _check_packed("k", k, q.shape)
+    _check_packed("v", v, q.shape)
+    _check_cu(cu_seqlens, q.device)
+    T, H, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, scale, stream)
+    return o, lse
 
 
 # ---------------------------------------------------------------- diagnostics

@@ -13,6 +13,9 @@ Recipe (the one reading of "N(0,1) from seed" used everywhere):
     (b, h) independently, ``randperm(S)[:round(0.01 * S)]`` picks 1 % of the
     key rows, which are multiplied by 8 (exact in bf16); V and dO are then
     drawn as usual.
+  * packed batches (sequences of different lengths back to back): the same
+    draw with B = 1 and S = the total token count, split by ``cu_seqlens``;
+    a length mix comes from ``packed_lengths`` (its own generator, seeded).
 """
 from __future__ import annotations
 
@@ -20,7 +23,7 @@ import math
 
 import torch
 
-__all__ = ["make_qkvdo", "default_scale", "WORKLOADS"]
+__all__ = ["make_qkvdo", "make_packed", "packed_lengths", "default_scale", "WORKLOADS"]
 
 
 def default_scale(D: int) -> float:
@@ -57,6 +60,25 @@ def make_qkvdo(B: int, H: int, S: int, D: int, seed: int = 0, stress: bool = Fal
 
 # The workloads the library is measured and checked on: (name, B, H, S, D,
 # causal list, stress).
+def packed_lengths(n: int, max_len: int, seed: int = 0, min_len: int = 1) -> list[int]:
+    """n sequence lengths drawn uniformly from [min_len, max_len] (seeded), the
+    first one max_len so that the longest sequence is exactly max_len."""
+    g = torch.Generator().manual_seed(seed)
+    rest = torch.randint(min_len, max_len + 1, (n - 1,), generator=g).tolist() if n > 1 else []
+    return [max_len] + rest
+
+
+def make_packed(lengths, H: int, D: int, seed: int = 0, stress: bool = False,
+                with_dout: bool = True):
+    """A packed batch: q, k, v (, dout) bf16 [T, H, D] with T = sum(lengths),
+    and cu_seqlens int32 [len(lengths) + 1] (CPU tensors)."""
+    T = int(sum(lengths))
+    q, k, v, do = make_qkvdo(1, H, T, D, seed=seed, stress=stress, with_dout=with_dout)
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.as_tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return q[0], k[0], v[0], (do[0] if do is not None else None), cu
+
+
 WORKLOADS = {
     "C1": dict(B=1, H=2, S=256, D=64, causal=(False,), stress=False),
     "C2": dict(B=4, H=16, S=2048, D=128, causal=(False,), stress=False),

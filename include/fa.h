@@ -90,6 +90,26 @@ fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float 
                     float rescale_threshold, int poly_exp2_groups, void *stream);
 
 /*
+ * Forward over a packed batch of sequences of different lengths (prefill
+ * style, the pages' integration target; [hyper]): sequence b holds the
+ * tokens [cu_seqlens[b], cu_seqlens[b+1]) of the packed tensors, and
+ * attention (and the causal mask) stays within each sequence.
+ *   q, k, v, o : bf16 [total, H, D] (token-major, like [B,S,H,D] with B = 1).
+ *   lse        : fp32 [H, total].
+ *   cu_seqlens : device int32 [B+1], 4-byte aligned, cu_seqlens[0] = 0,
+ *                non-decreasing, cu_seqlens[B] <= total; read on the device.
+ *   max_seqlen : >= every sequence's length, <= total (sizes the launch).
+ * A sequence whose offsets break these rules is skipped (its rows of o and
+ * lse are left as they were) and the device error word records
+ * 0x300 (see fa_device_error).  At tile edges the kernel reads rows of the
+ * neighbouring sequence and gives them zero weight, so all of k and v must
+ * be finite.  Errors otherwise as fa_fwd.
+ */
+fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                        const int *cu_seqlens, int B, int max_seqlen, int total, int H, int D,
+                        int causal, float scale, void *stream);
+
+/*
  * Bytes of caller-provided scratch the backward pass needs: the fp32 dQ
  * accumulator [B,H,S,D] followed by fp32 Delta [B,H,S], each rounded up to
  * 256 bytes.  Returns 0 for invalid sizes.
@@ -185,9 +205,11 @@ fa_status fa_last_cuda_error(int *cuda_err);
 
 /*
  * Synchronises the current device, then reports and (if clear != 0) resets
- * the device-side error word that bounded waits set when they run out.
- * *code = 0 means no wait ever ran out.  Returns FA_ERR_TIMEOUT when the
- * word is non-zero, FA_ERR_CUDA if the synchronisation fails.
+ * the device-side error word: the first error any kernel recorded.  0x1nn /
+ * 0x2nn: a bounded wait of the forward / backward kernel ran out (nn names
+ * the wait); 0x300: a packed batch's cu_seqlens broke its rules.  *code = 0
+ * means none.  Returns FA_ERR_TIMEOUT when the word is non-zero, FA_ERR_CUDA
+ * if the synchronisation fails.
  */
 fa_status fa_device_error(int *code, int clear);
 

@@ -334,16 +334,22 @@ size_t fa_bwd_workspace_size(int B, int H, int S, int D) {
 
 namespace {
 // fa_bwd and fa_bwd_deterministic; sem == nullptr selects the atomic-order dQ.
+// cu == nullptr: fixed length [B, S, H, D]; else a packed batch of B
+// sequences in [T, H, D] with S the longest.
 fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const void *dout,
                    const float *lse, float *dq_acc, float *delta, int *sem, void *dq, void *dk,
-                   void *dv, int B, int H, int S, int D, int causal, float scale, int pair_mode,
-                   void *stream) {
+                   void *dv, const int *cu, int B, int H, int S, int T, int D, int causal,
+                   float scale, int pair_mode, void *stream) {
     const void *ptrs[11] = {q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv};
     for (const void *p : ptrs)
         if (!p || !aligned16(p)) return FA_ERR_INVALID_ARG;
-    fa_status st = check_shape(B, H, S, D, scale);
+    fa_status st = cu ? check_shape(1, H, T, D, scale) : check_shape(B, H, S, D, scale);
     if (st != FA_OK) return st;
+    if (cu && (B < 1 || S < 1 || S > T || (reinterpret_cast<uintptr_t>(cu) & 3u)))
+        return FA_ERR_INVALID_ARG;
     if (pair_mode < -1 || pair_mode > 1) return FA_ERR_INVALID_ARG;
+    // packed batches: the single-CTA kernel (D = 64, 128), atomic-order dQ
+    if (cu && (D == 256 || sem || pair_mode == 1)) return FA_ERR_UNSUPPORTED;
     // CTA pairs: D = 128 with atomic-order dQ only.  Not the default: on
     // GB300 the single-CTA kernel is faster (the pair's dQ MMA, M = 128 over
     // two SMs, runs at half the per-SM tensor rate, and the dS exchange adds
@@ -359,11 +365,12 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     // drain warp its own), 32 x 64 on CTA pairs
     const unsigned qrows = D == 256 ? 64 : 128;
     const unsigned dqrows = pair ? 64 : 32;
-    if ((st = make_map_bshd(&a.tm_q, q, B, S, H, D, qrows)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_k, k, B, S, H, D)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_v, v, B, S, H, D)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_do, dout, B, S, H, D, qrows)) != FA_OK) return st;
-    if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, B * H, S, D, dqrows)) != FA_OK) return st;
+    const int mb = cu ? 1 : B, ms = cu ? T : S;  // the tensors' [B, S] as the maps see them
+    if ((st = make_map_bshd(&a.tm_q, q, mb, ms, H, D, qrows)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_k, k, mb, ms, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_v, v, mb, ms, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_do, dout, mb, ms, H, D, qrows)) != FA_OK) return st;
+    if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, mb * H, ms, D, dqrows)) != FA_OK) return st;
     if (pair) {
         if ((st = make_map_bshd(&a.tm_q64, q, B, S, H, D, 64)) != FA_OK) return st;
         if ((st = make_map_bshd(&a.tm_do64, dout, B, S, H, D, 64)) != FA_OK) return st;
@@ -387,6 +394,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     a.scale_log2 = scale * kLog2e;
     a.err_word = d->err_word;
     a.num_sms = d->num_sms;
+    a.cu_seqlens = cu;
+    a.T = cu ? T : B * S;
     cudaError_t e = fa::launch_bwd(a, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e);
@@ -399,16 +408,29 @@ extern "C" {
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
                  const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
                  int B, int H, int S, int D, int causal, float scale, void *stream) {
-    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, B, H, S, D,
-                    causal, scale, -1, stream);
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, nullptr, B, H, S,
+                    0, D, causal, scale, -1, stream);
 }
 
 fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
                     const float *lse, float *dq_acc, float *delta, void *dq, void *dk, void *dv,
                     int B, int H, int S, int D, int causal, float scale, int pair_mode,
                     void *stream) {
-    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, B, H, S, D,
-                    causal, scale, pair_mode, stream);
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, nullptr, B, H, S,
+                    0, D, causal, scale, pair_mode, stream);
+}
+
+size_t fa_bwd_varlen_workspace_size(int total, int H, int D) {
+    return fa_bwd_workspace_size(1, H, total, D);
+}
+
+fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                        const void *dout, const float *lse, float *dq_acc, float *delta, void *dq,
+                        void *dk, void *dv, const int *cu_seqlens, int B, int max_seqlen,
+                        int total, int H, int D, int causal, float scale, void *stream) {
+    if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, cu_seqlens, B, H,
+                    max_seqlen, total, D, causal, scale, 0, stream);
 }
 
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D) {
@@ -422,8 +444,8 @@ fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, cons
                                int *dq_sem, void *dq, void *dk, void *dv, int B, int H, int S,
                                int D, int causal, float scale, void *stream) {
     if (!dq_sem || !aligned16(dq_sem)) return FA_ERR_INVALID_ARG;
-    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, B, H, S, D,
-                    causal, scale, 0, stream);
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, nullptr, B, H, S,
+                    0, D, causal, scale, 0, stream);
 }
 
 fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream) {

@@ -265,6 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             if (!bunit_at(it, U, BH, un)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
+            if (!sp.ok && un.j == 0 && h == 0 && lane == 0)
+                atomicCAS(args.err_word, 0, kErrSeqlens);
+            if (un.j * kBlk >= sp.len) continue;  // past this sequence's end
+            const int nb = (sp.len + kBlk - 1) / kBlk;
             const int i0 = first_block(un.j, args.causal);
             if (lane == 0) {
                 w.code = kErrBwdWait + 1;
@@ -273,25 +278,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
                     for (int c = 0; c < Cfg::kBoxes; ++c) {
                         tma_load_4d(smem + Cfg::kOffK + c * kBox, &args.tm_k, kv_full, 64 * c, h,
-                                    un.j * kBlk, b);
+                                    sp.trow0 + un.j * kBlk, sp.tb);
                         tma_load_4d(smem + Cfg::kOffV + c * kBox, &args.tm_v, kv_full, 64 * c, h,
-                                    un.j * kBlk, b);
+                                    sp.trow0 + un.j * kBlk, sp.tb);
                     }
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             ++nunit;
-            for (int i = i0; i < nT && ok; ++i, ++nblk) {
+            for (int i = i0; i < nb && ok; ++i, ++nblk) {
                 const int st = nblk & 1;
                 // this block's -LSE/scale and -Delta per query, loaded before the
                 // waits so their latency overlaps them (-inf / 0 past S: P = 0)
-                const size_t rbase = static_cast<size_t>(un.bh) * S;
                 float lv[4], dv[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int q = i * kBlk + r * 32 + lane;
-                    lv[r] = q < S ? -args.lse[rbase + q] * inv_scale : -INFINITY;
-                    dv[r] = q < S ? -args.delta[rbase + q] : 0.f;
+                    const size_t x = stat_index(args.cu_seqlens, args.T, S, H, b, h, sp, q);
+                    lv[r] = q < sp.len ? -args.lse[x] * inv_scale : -INFINITY;
+                    dv[r] = q < sp.len ? -args.delta[x] : 0.f;
                 }
                 // Q_i into stage st, then the bias rows of S^T
                 w.code = kErrBwdWait + 2;
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     mbar_arrive_expect_tx(&q_full[st], Cfg::kTile);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_4d(smem + Cfg::kOffQ + st * Cfg::kTile + c * kBox, &args.tm_q,
-                                    &q_full[st], 64 * c, h, i * kBlk, b);
+                                    &q_full[st], 64 * c, h, sp.trow0 + i * kBlk, sp.tb);
                 }
                 uint8_t *lb = smem + Cfg::kOffLb + st * Cfg::kBias;
 #pragma unroll
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     mbar_arrive_expect_tx(do_full, Cfg::kTile);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_4d(smem + Cfg::kOffDO + c * kBox, &args.tm_do, do_full,
-                                    64 * c, h, i * kBlk, b);
+                                    64 * c, h, sp.trow0 + i * kBlk, sp.tb);
                 }
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
@@ -363,6 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 BUnit un;
                 if (!bunit_at(it, U, BH, un)) break;
                 if (un.j < 0) continue;
+                const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
+                if (un.j * kBlk >= sp.len) continue;
+                const int nb = (sp.len + kBlk - 1) / kBlk;
                 const int i0 = first_block(un.j, args.causal);
                 FA_WAIT(kv_full, nunit & 1, 10);
                 if (!ok) break;
@@ -387,9 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     issue_kmajor<D>(tY, aV, aDO, aOnes, aDb);
                     mma_commit(dp_full);
                 }
-                for (int i = i0; i < nT; ++i, ++nblk) {
+                for (int i = i0; i < nb; ++i, ++nblk) {
                     const int st = nblk & 1;
-                    const bool first = (i == i0), has_next = (i + 1 < nT);
+                    const bool first = (i == i0), has_next = (i + 1 < nb);
                     FA_WAIT(p_ready, ph_p, 14);
                     if (!ok) break;
                     ph_p ^= 1;
@@ -455,9 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             BUnit un;
             if (!bunit_at(it, U, BH, un)) break;
             if (un.j < 0) continue;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
+            if (un.j * kBlk >= sp.len) continue;
+            const int nb = (sp.len + kBlk - 1) / kBlk;
             const int i0 = first_block(un.j, args.causal);
-            const int key = un.j * kBlk + kr;
-            for (int i = i0; i < nT; ++i, ++n) {
+            const int key = un.j * kBlk + kr;  // row within the sequence
+            for (int i = i0; i < nb; ++i, ++n) {
                 w.code = kErrBwdWait + 31;
                 if (!mbar_wait(s_full, n & 1, w)) { ok = false; break; }
                 tc_fence_after();
@@ -473,9 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     // only where a block can hold invisible pairs: the causal
                     // diagonal block and a key tile reaching past S (queries past
                     // S carry a bias of -inf, which gives P = 0)
-                    if ((args.causal && i == un.j) || (un.j + 1) * kBlk > S) {
+                    if ((args.causal && i == un.j) || (un.j + 1) * kBlk > sp.len) {
                         const int lim = (args.causal && i == un.j) ? kr : -1;  // col < lim hidden
-                        const bool key_ok = key < S;
+                        const bool key_ok = key < sp.len;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -565,8 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             if (!bunit_at(it, U, BH, un)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
+            if (un.j * kBlk >= sp.len) continue;
+            const int nb = (sp.len + kBlk - 1) / kBlk;
+            // accumulator rows: [B*H, S] fixed, [H, T] packed
+            const int acc_row0 = args.cu_seqlens ? sp.tok0 : 0;
+            const int acc_z = args.cu_seqlens ? h : un.bh;
             const int i0 = first_block(un.j, args.causal);
-            for (int i = i0; i < nT; ++i, ++n) {
+            for (int i = i0; i < nb; ++i, ++n) {
                 w.code = kErrBwdWait + 40;
                 if (!mbar_wait(dq_full, n & 1, w)) { ok = false; break; }
                 tc_fence_after();
@@ -611,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && go && !*abort_flag) {
-                        tma_reduce_add_3d(&args.tm_dqacc, stage, 32 * c, i * kBlk + quarter * 32,
-                                          un.bh);
+                        tma_reduce_add_3d(&args.tm_dqacc, stage, 32 * c,
+                                          acc_row0 + i * kBlk + quarter * 32, acc_z);
                         bulk_commit();
                     }
                 }
@@ -632,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             ++nunit;
             tc_fence_after();
             const int key = un.j * kBlk + r;
-            const size_t orow = ((static_cast<size_t>(b) * S + key) * H + h) * D;
+            const size_t orow = ((static_cast<size_t>(sp.tok0) + key) * H + h) * D;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
@@ -648,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
                                             __uint_as_float(v[2 * e + 1]) * mul);
-                    if (key < S) {
+                    if (key < sp.len) {
                         uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4)
@@ -731,14 +748,21 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_cvt(const __grid_constant__ Bwd
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     using Cfg = BwdCfg<D>;
-    const long long rows = static_cast<long long>(a.B) * a.H * a.S;
+    // Delta, the accumulator and dQ are per token: the prep and convert
+    // kernels see a packed batch as one sequence of T tokens
+    BwdArgs rows_view = a;
+    if (a.cu_seqlens) {
+        rows_view.B = 1;
+        rows_view.S = a.T;
+    }
+    const long long rows = static_cast<long long>(rows_view.B) * a.H * rows_view.S;
     const long long blocks = (rows * 32 + 255) / 256;
-    fa_bwd_prep<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    fa_bwd_prep<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(rows_view);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.pair) {
         if ((e = launch_bwd_main_pair(a, stream)) != cudaSuccess) return e;
-        fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+        fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(rows_view);
         return cudaGetLastError();
     }
     auto kern = fa_bwd_kernel<D>;
@@ -757,7 +781,7 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
         kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(rows_view);
     return cudaGetLastError();
 }
 
@@ -768,7 +792,8 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
         case 64: return launch_bwd_d<64>(a, stream);
         case 128: return launch_bwd_d<128>(a, stream);
         case 256: {
-            if (a.dq_sem) return cudaErrorNotSupported;  // no ordered dQ at D = 256 yet
+            // no ordered dQ and no packed batches at D = 256 yet
+            if (a.dq_sem || a.cu_seqlens) return cudaErrorNotSupported;
             const long long rows = static_cast<long long>(a.B) * a.H * a.S;
             const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
             fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(a);

@@ -52,6 +52,9 @@ def lib():
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp]
         L.fa_bwd_ex.argtypes = [vp] * 11 + [i, i, i, i, i, f, i, vp]
+        L.fa_bwd_varlen.argtypes = [vp] * 12 + [i, i, i, i, i, i, f, vp]
+        L.fa_bwd_varlen_workspace_size.argtypes = [i, i, i]
+        L.fa_bwd_varlen_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd_deterministic.argtypes = [vp] * 12 + [i, i, i, i, i, f, vp]
         L.fa_bwd_semaphore_bytes.argtypes = [i, i, i, i]
         L.fa_bwd_semaphore_bytes.restype = ctypes.c_size_t
@@ -61,7 +64,7 @@ def lib():
         L.fa_device_error.argtypes = [ctypes.POINTER(i), i]
         L.fa_exp2_eval.argtypes = [vp, vp, ll, i, vp]
         L.fa_exp2_sweep.argtypes = [f, f, i, vp, vp]
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_bwd", "fa_bwd_ex",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_bwd", "fa_bwd_ex", "fa_bwd_varlen",
                      "fa_bwd_deterministic",
                      "fa_last_cuda_error",
                      "fa_device_error",
@@ -118,6 +121,17 @@ def fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, scale
                                                 _ptr(cu_seqlens), B, int(max_seqlen), T, H, D,
                                                 int(bool(causal)), float(scale),
                                                 _stream(stream)))
+
+
+def bwd_varlen(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, cu_seqlens, max_seqlen: int,
+               causal: bool, scale: float, stream=None):
+    """fa_bwd_varlen on caller-provided tensors (packed [T, H, D] layout)."""
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    _check("fa_bwd_varlen", lib().fa_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq_acc), _ptr(delta),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B, int(max_seqlen), T, H, D,
+        int(bool(causal)), float(scale), _stream(stream)))
 
 
 def bwd_workspace_size(B: int, H: int, S: int, D: int) -> int:
@@ -236,6 +250,30 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
     lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, scale, stream)
     return o, lse
+
+
+def backward_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale: float | None = None, stream=None):
+    """Exact attention backward over a packed batch (the forward_varlen
+    layout).  Returns (dq, dk, dv), bf16 [T, H, D]."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_packed(name, t, q.shape)
+    _check_cu(cu_seqlens, q.device)
+    T, H, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, T) or not lse.is_contiguous():
+        raise ValueError("lse: expected contiguous fp32 [H, T]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    n = H * T
+    ws = torch.empty(int(lib().fa_bwd_varlen_workspace_size(T, H, D)), dtype=torch.uint8,
+                     device=q.device)
+    acc_bytes = (n * D * 4 + 255) // 256 * 256
+    dq_acc = ws[:acc_bytes].view(torch.float32)
+    delta = ws[acc_bytes:acc_bytes + n * 4].view(torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    bwd_varlen(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, cu_seqlens, max_seqlen, causal,
+               scale, stream)
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------- diagnostics

@@ -135,6 +135,22 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  int B, int H, int S, int D, int causal, float scale, void *stream);
 
 /*
+ * Backward over a packed batch (see fa_fwd_varlen): q, k, v, o, dout, dq, dk,
+ * dv bf16 [total, H, D]; lse fp32 [H, total] from fa_fwd_varlen; dq_acc fp32
+ * [H, total, D] and delta fp32 [H, total] scratch, fa_bwd_varlen_workspace_size
+ * bytes in all (carved like fa_bwd's).  cu_seqlens and max_seqlen as for the
+ * forward, with the same 0x300 report for bad offsets.  D = 64 and 128;
+ * D = 256 returns FA_ERR_UNSUPPORTED.  Other arguments, results and errors as
+ * fa_bwd.
+ */
+size_t fa_bwd_varlen_workspace_size(int total, int H, int D);
+fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                        const void *dout, const float *lse, float *dq_acc, float *delta,
+                        void *dq, void *dk, void *dv, const int *cu_seqlens, int B,
+                        int max_seqlen, int total, int H, int D, int causal, float scale,
+                        void *stream);
+
+/*
  * Backward with the choice of main kernel ([nl] Methodologie §3: the 2-CTA
  * MMA mode splits operand B between two CTAs, and the pair exchanges halves
  * of the dQ work through distributed shared memory).

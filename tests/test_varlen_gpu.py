@@ -9,7 +9,7 @@ import torch
 
 from exact_attention_36_gb300 import fa
 from exact_attention_36_gb300.inputs import make_packed, packed_lengths
-from tests._parity import check_forward
+from tests._parity import check_backward, check_forward
 
 pytestmark = pytest.mark.gpu
 
@@ -82,3 +82,65 @@ def test_bad_offsets_are_reported_and_skipped():
     assert (o[:200] == 7.0).all() and (lse[:, :200] == 7.0).all()
     _check_fwd_each(q[200:], k[200:], v[200:], torch.tensor([0, 100], dtype=torch.int32),
                     o[200:].cpu(), lse[:, 200:].cpu(), False, 0.125)
+
+
+def _bwd(lengths, H, D, causal, seed=0, stress=False):
+    q, k, v, do, cu = make_packed(lengths, H, D, seed=seed, stress=stress)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd, dod, cud = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu.cuda()
+    mx = max(lengths)
+    o, lse = fa.forward_varlen(qd, kd, vd, cud, mx, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward_varlen(qd, kd, vd, o, dod, lse, cud, mx, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    return q, k, v, do, cu, dq.cpu(), dk.cpu(), dv.cpu(), scale
+
+
+def _check_bwd_each(q, k, v, do, cu, dq, dk, dv, causal, scale):
+    for b in range(cu.numel() - 1):
+        a0, a1 = int(cu[b]), int(cu[b + 1])
+        if a1 == a0:
+            continue
+        sl = slice(a0, a1)
+        check_backward(q[None, sl], k[None, sl], v[None, sl], do[None, sl], dq[None, sl],
+                       dk[None, sl], dv[None, sl], causal, scale, heads=None)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_ragged_mix(D, causal):
+    lengths = [1, 127, 128, 129, 300, 2, 640, 257]
+    args = _bwd(lengths, 3, D, causal, seed=1)
+    _check_bwd_each(*args[:8], causal, args[8])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_random_lengths_and_stress(causal):
+    lengths = packed_lengths(10, 900, seed=6)
+    args = _bwd(lengths, 2, 128, causal, seed=6, stress=True)
+    _check_bwd_each(*args[:8], causal, args[8])
+
+
+def test_backward_matches_fixed_length_kernel():
+    B, H, S, D = 3, 4, 700, 128
+    q, k, v, do, cu = make_packed([S] * B, H, D, seed=5)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.forward_varlen(qd, kd, vd, cu.cuda(), S, causal=True)
+    dq, dk, dv = fa.backward_varlen(qd, kd, vd, o, dod, lse, cu.cuda(), S, causal=True)
+    shp = (B, S, H, D)
+    o2, lse2 = fa.forward(qd.view(shp), kd.view(shp), vd.view(shp), causal=True)
+    dq2, dk2, dv2 = fa.backward(qd.view(shp), kd.view(shp), vd.view(shp), o2, dod.view(shp), lse2,
+                                causal=True)
+    torch.cuda.synchronize()
+    # dK, dV are reduced in a fixed order in both; dQ's fp32 sums run in
+    # atomic order
+    assert torch.equal(dk.view(shp), dk2) and torch.equal(dv.view(shp), dv2)
+    assert ((dq.view(shp).float() - dq2.float()).norm() / dq2.float().norm()).item() <= 1e-3
+
+
+def test_backward_rejects_what_it_does_not_cover():
+    q = torch.zeros(256, 2, 256, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 100, 256], dtype=torch.int32, device="cuda")
+    o, lse = fa.forward_varlen(q, q, q, cu, 156)
+    with pytest.raises(fa.FAError, match="UNSUPPORTED"):
+        fa.backward_varlen(q, q, q, o, q, lse, cu, 156)

@@ -71,7 +71,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -337,7 +337,7 @@ def recorded_traffic(kernel):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
@@ -423,15 +423,15 @@ def main():
 
     with ClockSampler(local_rank) as clk:
         ms, fwd_ms, bwd_ms = time_device(buf, False, scale, args.steps, args.warmup, dist_on)
+        if args.only_noncausal:
+            ms_c = fwd_ms_c = bwd_ms_c = float("nan")
+            e2e_ms, h2d, d2h = float("nan"), 0, 0
+        else:
+            ms_c, fwd_ms_c, bwd_ms_c = time_device(buf, True, scale, args.steps, args.warmup,
+                                                   dist_on)
+            e2e_ms, h2d, d2h = time_e2e(q, k, v, do, buf, False, scale, args.steps,
+                                        args.warmup, dist_on)
     clocks = clk.summary()
-    if args.only_noncausal:
-        ms_c = fwd_ms_c = bwd_ms_c = float("nan")
-        e2e_ms, h2d, d2h = float("nan"), 0, 0
-    else:
-        ms_c, fwd_ms_c, bwd_ms_c = time_device(buf, True, scale, args.steps, args.warmup,
-                                               dist_on)
-        e2e_ms, h2d, d2h = time_e2e(q, k, v, do, buf, False, scale, args.steps, args.warmup,
-                                    dist_on)
     assert fa.device_error() == 0, "a bounded device wait ran out"
 
     ff, fb = flops(B, H, S, D, False)

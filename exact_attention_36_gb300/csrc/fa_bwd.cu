@@ -78,7 +78,7 @@ struct BwdCfg {
     static constexpr int kOffBar = kOffDb + kBias;
     // kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full,
     // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dkdv_empty, drain
-    static constexpr int kNumBars = 17;
+    static constexpr int kNumBars = 18;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     // no alignment slack: the dynamic shared memory base must be 1024-byte
     // aligned (checked at kernel entry)
@@ -117,6 +117,35 @@ __device__ __forceinline__ bool bunit_at(int it, int U, int BH, BUnit &out) {
 
 // first query block a key tile sees (causal: queries >= first key)
 __device__ __forceinline__ int first_block(int j, int causal) { return causal ? j : 0; }
+
+// Query block a key tile visits at its step s.  Ascending from the first
+// visible block, except in the fixed-order mode without a causal mask, where
+// tile j starts at block j (rotated): the tiles that run together then reach
+// each block one step apart, which is the order their contributions to it
+// are fixed in (dq_position).
+__device__ __forceinline__ int block_at(int j, int s, int i0, int nb, bool rotate) {
+    return rotate ? (j + s) % nb : i0 + s;
+}
+
+// Fixed-order mode: the place of key tile j's contribution in the sum of dQ
+// block i (0 = first).  Units are numbered head by head (unit u = bh nT + j)
+// and taken in rounds of G by the persistent grid; [j0, j1) are the head's
+// tiles in j's round.  Contributions of earlier rounds come first; within a
+// round they are ordered by the step at which each tile reaches block i, so
+// every wait points to a unit of the same round or an earlier one (no cycle),
+// and in the same round to the tile one step ahead.
+__device__ __forceinline__ int dq_position(int bh, int j, int i, int nT, int G, bool causal) {
+    const int r = (bh * nT + j) / G;
+    const int j0 = max(r * G - bh * nT, 0), j1 = min((r + 1) * G - bh * nT, nT);
+    if (causal)  // tiles j' <= i, reached at step i - j'
+        return min(i + 1, j0) + (min(i, j1 - 1) - j);
+    // every tile sees every block, reached at step (i - j') mod nT: earlier
+    // steps are the tiles in the circular range (j, i]
+    auto in_round = [&](int lo, int hi) { return max(0, min(j1, hi) - max(j0, lo)); };
+    const int ahead = j < i ? in_round(j + 1, i + 1)
+                            : (j > i ? in_round(j + 1, nT) + in_round(0, i + 1) : 0);
+    return j0 + ahead;
+}
 
 // ---------------------------------------------------------------- MMA helpers
 
@@ -178,7 +207,9 @@ __device__ __forceinline__ void issue_dq(uint32_t tD, uint32_t ds_saddr, uint32_
 
 // ---------------------------------------------------------------- main kernel
 
-template <int D>
+// kDet: the fixed-order dQ mode (args.dq_sem set), a separate instance so
+// that the atomic-order kernel carries none of its logic
+template <int D, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdArgs args) {
     using Cfg = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -196,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     uint64_t *dq_full = bars + 12, *dq_empty = bars + 13;
     uint64_t *dkdv_full = bars + 14, *dkdv_empty = bars + 15;
     uint64_t *drain = bars + 16;
+    uint64_t *rel_bar = bars + 17;  // fixed-order mode: the four drain warps' reductions done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
@@ -206,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     const int nT = (S + kBlk - 1) / kBlk;  // key tiles = query blocks
     const int U = BH * nT;
     const int nSem = (S + 63) / 64;        // deterministic-mode counters per head
+    const bool rotate = kDet && !args.causal;  // see block_at
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -225,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         mbar_init(dkdv_full, 1);
         mbar_init(dkdv_empty, 128);
         mbar_init(drain, 1);
+        mbar_init(rel_bar, 4);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -286,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             ++nunit;
-            for (int i = i0; i < nb && ok; ++i, ++nblk) {
+            for (int i_ = i0; i_ < nb && ok; ++i_, ++nblk) {
+                const int i = kDet ? block_at(un.j, i_ - i0, i0, nb, rotate) : i_;
                 const int st = nblk & 1;
                 // this block's -LSE/scale and -Delta per query, loaded before the
                 // waits so their latency overlaps them (-inf / 0 past S: P = 0)
@@ -468,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             const int nb = (sp.len + kBlk - 1) / kBlk;
             const int i0 = first_block(un.j, args.causal);
             const int key = un.j * kBlk + kr;  // row within the sequence
-            for (int i = i0; i < nb; ++i, ++n) {
+            for (int i_ = i0; i_ < nb; ++i_, ++n) {
+                const int i = kDet ? block_at(un.j, i_ - i0, i0, nb, rotate) : i_;
                 w.code = kErrBwdWait + 31;
                 if (!mbar_wait(s_full, n & 1, w)) { ok = false; break; }
                 tc_fence_after();
@@ -569,6 +605,43 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         uint8_t *stage = smem + Cfg::kOffRed + quarter * 4096;
         uint8_t *stage_row = stage + lane * 128;
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 40};
+        // fixed-order mode: one block's contribution is complete in L2 in all
+        // four warps (each arrives on rel_bar and waits, bounded, for the
+        // other three, so no warp runs a block ahead), then the leader
+        // advances the block's counter
+        // each warp stages its 32 query rows of dQ_i, 32 columns at a time, and
+        // reduces them on its own (no wait on the other drain warps)
+        auto stage_and_reduce = [&](const uint32_t (&acc)[D], int row0, int z, bool go) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                if (lane == 0) bulk_wait_read<0>();  // the previous reduction has read buf
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4 *>(stage_row + ((k ^ (lane & 7)) << 4)) =
+                        make_uint4(acc[c * 32 + 4 * k], acc[c * 32 + 4 * k + 1],
+                                   acc[c * 32 + 4 * k + 2], acc[c * 32 + 4 * k + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && go && !*abort_flag) {
+                    tma_reduce_add_3d(&args.tm_dqacc, stage, 32 * c, row0, z);
+                    bulk_commit();
+                }
+            }
+        };
+        int *sem_prev = nullptr;
+        uint32_t nrel = 0;
+        auto release_block = [&](int *sem_done) {
+            if (lane == 0) {
+                bulk_wait<0>();
+                fence_proxy_async_global();
+                __threadfence();
+                mbar_arrive(rel_bar);
+                w.code = kErrBwdWait + 43;
+                if (mbar_wait(rel_bar, nrel & 1, w) && leader) red_release_gpu_add(sem_done, 1);
+            }
+            ++nrel;
+        };
         uint32_t n = 0, nunit = 0;
         bool ok = true;
         for (int it = 0; ok; ++it) {
@@ -583,7 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             const int acc_row0 = args.cu_seqlens ? sp.tok0 : 0;
             const int acc_z = args.cu_seqlens ? h : un.bh;
             const int i0 = first_block(un.j, args.causal);
-            for (int i = i0; i < nb; ++i, ++n) {
+            for (int i_ = i0; i_ < nb; ++i_, ++n) {
+                const int i = kDet ? block_at(un.j, i_ - i0, i0, nb, rotate) : i_;
                 w.code = kErrBwdWait + 40;
                 if (!mbar_wait(dq_full, n & 1, w)) { ok = false; break; }
                 tc_fence_after();
@@ -597,51 +671,62 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&acc[c * 32]));
                 tc_fence_before();
                 mbar_arrive(dq_empty);
-                // deterministic mode: key tile j adds its share of dQ block i only
-                // after tiles 0 .. j-1 have (they are the only tiles before it
-                // that see block i), so every sum runs in key order.  A tile only
-                // ever waits on a smaller unit index (an earlier or concurrent
-                // unit), so the waits cannot form a cycle.
-                int *sem = args.dq_sem ? args.dq_sem + static_cast<size_t>(un.bh) * nSem +
-                                             (i * kBlk) / 64
-                                       : nullptr;
-                bool go = true;
-                if (sem) {
+                if constexpr (kDet) {
+                    // Fixed order: key tile j adds its share of dQ block i when
+                    // the block's counter reaches its place in the sum
+                    // (dq_position).  The previous block's counter is released
+                    // first, a block period after its reductions were issued (so
+                    // they are complete) and independently of this block's wait:
+                    // releases follow only this CTA's own progress, which keeps
+                    // the waits between tiles acyclic.
+                    if (sem_prev) {
+                        release_block(sem_prev);
+                        sem_prev = nullptr;
+                    }
+                    int *sem = args.dq_sem + static_cast<size_t>(un.bh) * nSem + (i * kBlk) / 64;
+                    bool go = true;
                     if (lane == 0) {
                         w.code = kErrBwdWait + 42;
-                        go = counter_wait_geq(sem, un.j, w);
+                        go = counter_wait_geq(
+                            sem, dq_position(un.bh, un.j, i, nT, gridDim.x, args.causal != 0), w);
                         fence_proxy_async_global();
                     }
                     go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-                }
-                // each warp stages its 32 query rows, 32 columns at a time, and
-                // reduces them on its own (no wait on the other drain warps)
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    if (lane == 0) bulk_wait_read<0>();  // the previous reduction has read buf
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<uint4 *>(stage_row + ((k ^ (lane & 7)) << 4)) =
-                            make_uint4(acc[c * 32 + 4 * k], acc[c * 32 + 4 * k + 1],
-                                       acc[c * 32 + 4 * k + 2], acc[c * 32 + 4 * k + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && go && !*abort_flag) {
-                        tma_reduce_add_3d(&args.tm_dqacc, stage, 32 * c,
-                                          acc_row0 + i * kBlk + quarter * 32, acc_z);
-                        bulk_commit();
+                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, go);
+                    sem_prev = sem;
+                } else {
+                    // Atomic order.  This instance is launched only without
+                    // dq_sem, so the sem branches below never run; they are kept
+                    // because ptxas allocates the kernel's registers differently
+                    // without them (36 instead of 4 bytes of spills), which
+                    // measured 2-3 % slower on GB300 (same-box A/B).
+                    int *sem = args.dq_sem ? args.dq_sem + static_cast<size_t>(un.bh) * nSem +
+                                                 (i * kBlk) / 64
+                                           : nullptr;
+                    bool go = true;
+                    if (sem) {
+                        if (lane == 0) {
+                            w.code = kErrBwdWait + 42;
+                            go = counter_wait_geq(sem, un.j, w);
+                            fence_proxy_async_global();
+                        }
+                        go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+                    }
+                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, go);
+                    if (sem) {
+                        if (lane == 0) {
+                            bulk_wait<0>();
+                            fence_proxy_async_global();
+                            __threadfence();
+                        }
+                        named_bar_sync(1, 128);
+                        if (leader) red_release_gpu_add(sem, 1);
                     }
                 }
-                if (sem) {
-                    if (lane == 0) {
-                        bulk_wait<0>();  // this warp's reductions are done in L2
-                        fence_proxy_async_global();
-                        __threadfence();
-                    }
-                    named_bar_sync(1, 128);  // and the other three warps'
-                    if (leader) red_release_gpu_add(sem, 1);
-                }
+            }
+            if (kDet && sem_prev) {  // the unit's last block
+                release_block(sem_prev);
+                sem_prev = nullptr;
             }
             if (!ok) break;
             w.code = kErrBwdWait + 41;
@@ -765,7 +850,7 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
         fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(rows_view);
         return cudaGetLastError();
     }
-    auto kern = fa_bwd_kernel<D>;
+    auto kern = a.dq_sem ? fa_bwd_kernel<D, true> : fa_bwd_kernel<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);

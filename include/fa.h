@@ -173,13 +173,15 @@ fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
 
 /*
  * Deterministic backward ([nl] Methodologie §3 and Belangrijkste Resultaten:
- * a deterministic mode ordered by semaphores): the same results as fa_bwd,
- * except that every element of dQ is summed over the key tiles in a fixed
- * order (key tile 0, 1, 2, ...), so repeated calls on the same inputs give
- * bitwise-identical dQ (dK and dV are already reduced in a fixed order).
- * The key tile that contributes to a 128-query block next waits on a per-block
- * counter; the kernel is launched cooperatively, so all its CTAs are resident
- * while they wait on one another.
+ * a deterministic mode ordered by semaphores and scheduling): the same
+ * results as fa_bwd to rounding, except that every element of dQ is summed
+ * over the key tiles in an order fixed by (B, H, S, causal) and the device's
+ * SM count, so repeated calls on the same inputs on the same GPU model give
+ * bitwise-identical dQ, dK and dV.  Each 128-query block has a counter; the
+ * key tile whose turn it is adds its share, and the order puts the tiles that
+ * run at the same time one step apart, so few of them wait.  The kernel is
+ * launched cooperatively, so all its CTAs are resident while they wait on one
+ * another.
  *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes (contents on
  *            entry ignored; the first launch zeroes it).
  * Other arguments, results and errors as fa_bwd.  D = 256 returns

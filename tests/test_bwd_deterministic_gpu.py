@@ -37,10 +37,15 @@ def test_deterministic_is_bitwise_repeatable_and_exact(B, H, S, D, causal):
     heads = [(0, 0), (B - 1, H - 1)]
     rows = None if S <= 1024 else sample_rows(S, 128, seed=6)
     check_backward(*cpu, *a, causal, scale, heads=heads, rows=rows, cols=rows)
-    # the atomic-order backward differs only by the order of fp32 additions
+    # the atomic-order backward differs only by the order of fp32 additions:
+    # dQ's, and without a causal mask (where the fixed order visits the query
+    # blocks rotated) dK's and dV's
     c = fa.backward(qd, kd, vd, o, dod, lse, causal, scale)
-    assert torch.equal(a[1], c[1]) and torch.equal(a[2], c[2])
-    assert (a[0].float() - c[0].float()).abs().max().item() <= 1e-2
+    if causal:
+        assert torch.equal(a[1], c[1]) and torch.equal(a[2], c[2])
+    for x, y in zip(a, c):
+        x, y = x.float(), y.float()
+        assert ((x - y).norm() / y.norm()).item() <= 2e-3
 
 
 def test_deterministic_long_context_sampled():

@@ -362,9 +362,9 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     fa::BwdArgs a;
     std::memset(&a, 0, sizeof(a));
     // D = 256 streams 64-query blocks; dQ is staged as 32 x 32 tiles (each
-    // drain warp its own), 32 x 64 on CTA pairs
+    // drain warp its own)
     const unsigned qrows = D == 256 ? 64 : 128;
-    const unsigned dqrows = pair ? 64 : 32;
+    const unsigned dqrows = 32;
     const int mb = cu ? 1 : B, ms = cu ? T : S;  // the tensors' [B, S] as the maps see them
     if ((st = make_map_bshd(&a.tm_q, q, mb, ms, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_k, k, mb, ms, H, D)) != FA_OK) return st;

@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             tc_fence_before();
             mbar_arrive(dkdv_empty);
         }
-        if (leader) bulk_wait<0>();
+        if (lane == 0) bulk_wait<0>();  // every drain warp's reductions have read shared memory
     }
 
     tc_fence_before();

@@ -62,10 +62,10 @@ struct PairCfg {
     static constexpr int kOffDOd = kOffDOs + 2 * kHalfBox;  // dV's B: 128 x 64 d
     static constexpr int kOffDS = kOffDOd + kBox;  // dQ's A: 256 keys x 64 queries bf16
     static constexpr int kOffDSx = kOffDS + 2 * kBox;  // the other CTA's dS half, outgoing
-    static constexpr int kOffRed = kOffDSx + kBox;     // dQ staging: 2 x (64 rows x 32 fp32)
+    static constexpr int kOffRed = kOffDSx + kBox;     // dQ staging: 4 warps x 32 x 32 fp32
     static constexpr int kOffStat = kOffRed + kBox;    // 2 x (128 lse2 + 128 delta) fp32
     static constexpr int kOffBar = kOffStat + 2 * 1024;
-    static constexpr int kNumBars = 26;
+    static constexpr int kNumBars = 27;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
@@ -80,7 +80,7 @@ static_assert(PairCfg::kSmemBytes <= 232448, "shared memory");
 enum PairBar : int {
     kKvFull, kKvEmpty, kQsFull, kQsEmpty, kQdFull, kQdEmpty, kDosFull, kDosEmpty, kDodFull,
     kDodEmpty, kSFull, kDpFull, kPReady, kDsReady, kDqFull, kDqEmpty, kDkdvFull, kDkdvEmpty,
-    kDrain, kPkKv, kPkQs, kPkQd, kPkDos, kPkDod, kDsIn, kPkDs
+    kDrain, kPkKv, kPkQs, kPkQd, kPkDos, kPkDod, kDsIn, kPkDs, kStaged
 };
 
 struct PUnit {
@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             1, 1, 2, 1, 1, 1, 1, 1, 1, 1,  // kv .. dod_empty
             1, 1, 8, 8, 1, 8, 1, 8,        // s_full .. dkdv_empty
             1, 1, 1, 1, 1, 1,              // drain, pk_*
-            1, 1};                         // ds_in (+ the other CTA's copy), pk_ds
+            1, 1,                          // ds_in (+ the other CTA's copy), pk_ds
+            4};                            // staged: the four softmax warps' dS rows
         for (int i = 0; i < Cfg::kNumBars; ++i) mbar_init(&bars[i], counts[i]);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -600,9 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tmem_st_wait();
                 tc_fence_before();
-                named_bar_sync(2, 128);  // all 128 rows staged
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kStaged]);  // this warp's 32 rows staged
                 if (copier) {
-                    // the other CTA's half arrives here in this block's phase
+                    // all 128 rows staged (bounded wait; the other warps do not
+                    // wait here); the other CTA's half arrives in this phase
+                    w.code = kErrBwdWait + 0xc4;
+                    if (!mbar_wait(&bars[kStaged], n & 1, w)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bars[kDsIn], kBox);
                     bulk_copy_to_cluster(ds_peer_rows, smem + Cfg::kOffDSx, kBox, ds_peer_bar);
                 }
@@ -615,14 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
         // This CTA's 64 queries of dQ_i: warps 8-9 hold d [0,64), warps 10-11
-        // d [64,128) (lanes 0-63 and 64-127 of the M = 128 pair result).  Two
-        // rounds of two 64 x 32 fp32 boxes, staged 128B-swizzled and added into
-        // the accumulator by TMA bulk reductions.
+        // d [64,128) (lanes 0-63 and 64-127 of the M = 128 pair result), each
+        // warp 32 query rows.  Each warp stages its rows as two 32 x 32 fp32
+        // tiles (128B-swizzled, 4 KB of its own) and adds them into the
+        // accumulator by TMA bulk reductions.
         const int quarter = warp & 3;
         const int half = quarter >> 1;
-        const int qr = (quarter & 1) * 32 + lane;  // query row within this CTA's 64
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const bool leader = (threadIdx.x == 256);
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0xd0};
         uint32_t n = 0, nunit = 0;
         bool ok = true;
@@ -647,26 +651,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(bar_dqe);
-                const int q0 = i * kBlk + 64 * static_cast<int>(rank);
+                // this warp's 32 query rows, its 64 columns in two 32 x 32
+                // tiles, staged in its own 4 KB and reduced on its own
+                const int q0 = i * kBlk + 64 * static_cast<int>(rank) + (quarter & 1) * 32;
+                uint8_t *buf = smem + Cfg::kOffRed + quarter * 4096;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    uint8_t *buf = smem + Cfg::kOffRed;
-                    if (leader) bulk_wait_read<0>();  // the previous reductions have read buf
-                    named_bar_sync(1, 128);
-                    uint8_t *row = buf + half * kHalfBox + qr * 128;
+                    if (lane == 0) bulk_wait_read<0>();  // the previous reduction has read buf
+                    __syncwarp();
+                    uint8_t *row = buf + lane * 128;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<uint4 *>(row + ((k ^ (qr & 7)) << 4)) =
+                        *reinterpret_cast<uint4 *>(row + ((k ^ (lane & 7)) << 4)) =
                             make_uint4(acc[t * 32 + 4 * k], acc[t * 32 + 4 * k + 1],
                                        acc[t * 32 + 4 * k + 2], acc[t * 32 + 4 * k + 3]);
                     fence_proxy_async_smem();
-                    named_bar_sync(1, 128);
-                    if (leader) {
-                        if (!*abort_flag) {
-                            tma_reduce_add_3d(&args.tm_dqacc, buf, 32 * t, q0, un.bh);
-                            tma_reduce_add_3d(&args.tm_dqacc, buf + kHalfBox, 64 + 32 * t, q0,
-                                              un.bh);
-                        }
+                    __syncwarp();
+                    if (lane == 0 && !*abort_flag) {
+                        tma_reduce_add_3d(&args.tm_dqacc, buf, half * 64 + 32 * t, q0, un.bh);
                         bulk_commit();
                     }
                 }
@@ -707,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(bar_dkdve);
         }
-        if (leader) bulk_wait<0>();
+        if (lane == 0) bulk_wait<0>();  // every drain warp's reductions have read shared memory
     }
 
     // neither CTA leaves (or releases Tensor Memory) while the other may still

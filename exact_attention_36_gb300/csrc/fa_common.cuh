@@ -34,8 +34,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [B,S,H,D], same boxes as the forward
-    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 32 x 1 (CTA pairs:
-                                          // 32 x 64 x 1)
+    CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 32 x 1
     CUtensorMap tm_q64, tm_do64;          // CTA pairs: Q and dO with 64-row boxes
     const void *o, *dout;                 // bf16 [B,S,H,D]
     const float *lse;                     // fp32 [B,H,S]

@@ -18,7 +18,8 @@
 // CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent over
 // work units):
 //   warp 0       TMA producer: Q tile pair, then K_j / V_j into a ring of
-//                shared-memory slots guarded by full/empty mbarriers.
+//                shared-memory slots guarded by full/empty mbarriers (with two
+//                query tiles, one barrier pair per group of slots {V_j, K_j+1}).
 //   warp 1       TMEM allocator and MMA issuer (one elected lane).
 //   warps 2-3    idle (they complete warpgroup 0).
 //   warps 4-7    softmax + epilogue of query tile 0.
@@ -57,6 +58,10 @@ struct FwdCfg {
     static constexpr int kNQ = (D == 256) ? 1 : 2;
     static constexpr int kRows = kBlockM * kNQ;          // query rows per work unit
     static constexpr int kStages = (D == 64) ? 8 : (D == 128 ? 4 : 2);  // ring slots
+    // With two query tiles the slots are used in groups of two, {V_j, K_j+1},
+    // each group with one full and one empty barrier (kv_full/kv_empty[g]).
+    static constexpr bool kGrouped = (kNQ == 2);
+    static constexpr int kGroups = kStages / 2;
     static constexpr int kQBytes = kNQ * kTileBytes;
     static constexpr int kRingOff = kQBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
@@ -211,29 +216,55 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_4d(smem + t * Cfg::kTileBytes + c * kBox, &args.tm_q, q_full,
                                     64 * c, h, sp.trow0 + un.p * Cfg::kRows + t * kBlockM, sp.tb);
-                for (int j = 0; j < n1 && ok; ++j) {
-                    for (int which = 0; which < 2; ++which) {
-                        const uint32_t slot = ring % Cfg::kStages;
-                        w.code = kErrFwdWait + 2;
-                        if (!mbar_wait(&kv_empty[slot], ((ring / Cfg::kStages) & 1) ^ 1, w)) {
+                if constexpr (Cfg::kGrouped) {
+                    // groups {K_0}, then {V_j, K_j+1} for j = 0 .. n1-1: one
+                    // full and one empty barrier per group of two slots
+                    for (int j = -1; j < n1 && ok; ++j) {
+                        const uint32_t g = ring % Cfg::kGroups;
+                        w.code = kErrFwdWait + 3;
+                        if (!mbar_wait(&kv_empty[g], ((ring / Cfg::kGroups) & 1) ^ 1, w)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&kv_full[slot], Cfg::kTileBytes);
-                        uint8_t *dst = smem + Cfg::kRingOff + slot * Cfg::kTileBytes;
-                        const CUtensorMap *map = which ? &args.tm_v : &args.tm_k;
-                        for (int c = 0; c < Cfg::kBoxes; ++c)
-                            tma_load_4d(dst + c * kBox, map, &kv_full[slot], 64 * c, h,
-                                        sp.trow0 + j * kBlockN, sp.tb);
+                        const bool has_v = j >= 0, has_k = j + 1 < n1;
+                        mbar_arrive_expect_tx(&kv_full[g], Cfg::kTileBytes * ((has_v ? 1 : 0) + (has_k ? 1 : 0)));
+                        uint8_t *dst = smem + Cfg::kRingOff + 2 * g * Cfg::kTileBytes;
+                        for (int c = 0; c < Cfg::kBoxes; ++c) {
+                            if (has_v)
+                                tma_load_4d(dst + c * kBox, &args.tm_v, &kv_full[g], 64 * c, h,
+                                            sp.trow0 + j * kBlockN, sp.tb);
+                            if (has_k)
+                                tma_load_4d(dst + Cfg::kTileBytes + c * kBox, &args.tm_k, &kv_full[g],
+                                            64 * c, h, sp.trow0 + (j + 1) * kBlockN, sp.tb);
+                        }
                         ++ring;
+                    }
+                } else {
+                    for (int j = 0; j < n1 && ok; ++j) {
+                        for (int which = 0; which < 2; ++which) {
+                            const uint32_t slot = ring % Cfg::kStages;
+                            w.code = kErrFwdWait + 2;
+                            if (!mbar_wait(&kv_empty[slot], ((ring / Cfg::kStages) & 1) ^ 1, w)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&kv_full[slot], Cfg::kTileBytes);
+                            uint8_t *dst = smem + Cfg::kRingOff + slot * Cfg::kTileBytes;
+                            const CUtensorMap *map = which ? &args.tm_v : &args.tm_k;
+                            for (int c = 0; c < Cfg::kBoxes; ++c)
+                                tma_load_4d(dst + c * kBox, map, &kv_full[slot], 64 * c, h,
+                                            sp.trow0 + j * kBlockN, sp.tb);
+                            ++ring;
+                        }
                     }
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
-                const uint32_t lo = ring > (uint32_t)Cfg::kStages ? ring - Cfg::kStages : 0;
+                constexpr uint32_t kBufs = Cfg::kGrouped ? Cfg::kGroups : Cfg::kStages;
+                const uint32_t lo = ring > kBufs ? ring - kBufs : 0;
                 for (uint32_t r = lo; r < ring; ++r)
-                    mbar_wait_drain(&kv_full[r % Cfg::kStages], (r / Cfg::kStages) & 1);
+                    mbar_wait_drain(&kv_full[r % kBufs], (r / kBufs) & 1);
                 if (qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
             }
         }
@@ -259,72 +290,91 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 w.code = kErrFwdWait + 10;
                 if (!mbar_wait(q_full, qi & 1, w)) { ok = false; break; }
                 ++qi;
-                const uint32_t kslot = ring % Cfg::kStages;
-                w.code = kErrFwdWait + 11;
-                if (!mbar_wait(&kv_full[kslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
-                ++ring;
-                tc_fence_after();
-                issue_qk<D>(tS0, q0, ring_base + kslot * Cfg::kTileBytes);
-                mma_commit(&s_full[0]);
-                if constexpr (Cfg::kNQ == 2) {
-                    issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
-                    mma_commit(&s_full[1]);
-                }
-                mma_commit(&kv_empty[kslot]);
-                for (int j = 0; j < n1; ++j) {
-                    const uint32_t vslot = ring % Cfg::kStages;
-                    w.code = kErrFwdWait + 12;
-                    if (!mbar_wait(&kv_full[vslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                if constexpr (Cfg::kGrouped) {
+                    // Between two MMA groups the tensor pipe holds about one
+                    // queued MMA, so every wait or commit placed there idles it:
+                    // per key tile this issues [wait group, wait P0] PV0 S0
+                    // [commit, wait P1] PV1 S1 [commit, commit].
+                    uint32_t g = ring % Cfg::kGroups;
+                    w.code = kErrFwdWait + 11;
+                    if (!mbar_wait(&kv_full[g], (ring / Cfg::kGroups) & 1, w)) { ok = false; break; }
                     ++ring;
-                    const bool has_next = (j + 1 < n1);
-                    uint32_t nslot = 0, nphase = 0;
-                    if (has_next) {
-                        nslot = ring % Cfg::kStages;
-                        nphase = (ring / Cfg::kStages) & 1;
+                    tc_fence_after();
+                    uint32_t kaddr = ring_base + (2 * g + 1) * Cfg::kTileBytes;
+                    issue_qk<D>(tS0, q0, kaddr);
+                    mma_commit(&s_full[0]);
+                    issue_qk<D>(tS1, q1, kaddr);
+                    mma_commit(&s_full[1]);
+                    mma_commit(&kv_empty[g]);
+                    for (int j = 0; j < n1; ++j) {
+                        g = ring % Cfg::kGroups;
+                        w.code = kErrFwdWait + 12;
+                        if (!mbar_wait(&kv_full[g], (ring / Cfg::kGroups) & 1, w)) { ok = false; break; }
                         ++ring;
+                        const uint32_t vaddr = ring_base + 2 * g * Cfg::kTileBytes;
+                        kaddr = vaddr + Cfg::kTileBytes;
+                        if (j < n0) {
+                            w.code = kErrFwdWait + 13;
+                            if (!mbar_wait(&p_full[0], pph0, w)) { ok = false; break; }
+                            pph0 ^= 1;
+                            tc_fence_after();
+                            issue_pv<D>(tO0, tS0, vaddr, j > 0);
+                            if (j + 1 < n0) {
+                                issue_qk<D>(tS0, q0, kaddr);
+                                mma_commit(&s_full[0]);
+                            } else {
+                                mma_commit(&o_full[0]);
+                            }
+                        }
+                        w.code = kErrFwdWait + 15;
+                        if (!mbar_wait(&p_full[1], pph1, w)) { ok = false; break; }
+                        pph1 ^= 1;
+                        tc_fence_after();
+                        issue_pv<D>(tO1, tS1, vaddr, j > 0);
+                        if (j + 1 < n1) {
+                            issue_qk<D>(tS1, q1, kaddr);
+                            mma_commit(&s_full[1]);
+                        } else {
+                            mma_commit(&o_full[1]);
+                            mma_commit(q_empty);
+                        }
+                        mma_commit(&kv_empty[g]);
                     }
-                    const uint32_t vaddr = ring_base + vslot * Cfg::kTileBytes;
-                    const uint32_t naddr = ring_base + nslot * Cfg::kTileBytes;
-                    bool next_ready = false;
-                    if (j < n0) {
+                } else {
+                    // one query tile (D = 256): K_j and V_j in single slots,
+                    // per key tile PV(j), then S(j+1)
+                    const uint32_t kslot = ring % Cfg::kStages;
+                    w.code = kErrFwdWait + 11;
+                    if (!mbar_wait(&kv_full[kslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                    ++ring;
+                    tc_fence_after();
+                    issue_qk<D>(tS0, q0, ring_base + kslot * Cfg::kTileBytes);
+                    mma_commit(&s_full[0]);
+                    mma_commit(&kv_empty[kslot]);
+                    for (int j = 0; j < n0; ++j) {
+                        const uint32_t vslot = ring % Cfg::kStages;
+                        w.code = kErrFwdWait + 12;
+                        if (!mbar_wait(&kv_full[vslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                        ++ring;
                         w.code = kErrFwdWait + 13;
                         if (!mbar_wait(&p_full[0], pph0, w)) { ok = false; break; }
                         pph0 ^= 1;
                         tc_fence_after();
-                        issue_pv<D>(tO0, tS0, vaddr, j > 0);
-                        if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[vslot]);
+                        issue_pv<D>(tO0, tS0, ring_base + vslot * Cfg::kTileBytes, j > 0);
+                        mma_commit(&kv_empty[vslot]);
                         if (j + 1 < n0) {
+                            const uint32_t nslot = ring % Cfg::kStages;
                             w.code = kErrFwdWait + 14;
-                            if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
-                            next_ready = true;
+                            if (!mbar_wait(&kv_full[nslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                            ++ring;
                             tc_fence_after();
-                            issue_qk<D>(tS0, q0, naddr);
+                            issue_qk<D>(tS0, q0, ring_base + nslot * Cfg::kTileBytes);
                             mma_commit(&s_full[0]);
-                            if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[nslot]);
+                            mma_commit(&kv_empty[nslot]);
                         } else {
                             mma_commit(&o_full[0]);
-                            if constexpr (Cfg::kNQ == 1) mma_commit(q_empty);
+                            mma_commit(q_empty);
                         }
-                    }
-                    if constexpr (Cfg::kNQ == 1) continue;
-                    w.code = kErrFwdWait + 15;
-                    if (!mbar_wait(&p_full[1], pph1, w)) { ok = false; break; }
-                    pph1 ^= 1;
-                    tc_fence_after();
-                    issue_pv<D>(tO1, tS1, vaddr, j > 0);
-                    mma_commit(&kv_empty[vslot]);
-                    if (has_next) {
-                        if (!next_ready) {
-                            w.code = kErrFwdWait + 16;
-                            if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
-                            tc_fence_after();
-                        }
-                        issue_qk<D>(tS1, q1, naddr);
-                        mma_commit(&s_full[1]);
-                        mma_commit(&kv_empty[nslot]);
-                    } else {
-                        mma_commit(&o_full[1]);
-                        mma_commit(q_empty);
                     }
                 }
             }

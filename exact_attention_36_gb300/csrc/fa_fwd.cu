@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     // Between two MMA groups the tensor pipe holds about one
                     // queued MMA, so every wait or commit placed there idles it:
                     // per key tile this issues [wait group, wait P0] PV0 S0
-                    // [commit, wait P1] PV1 S1 [commit, commit].
+                    // [commit, wait P1] PV1 S1 [commit].  Groups are released by
+                    // the softmax of tile 1 (S1(j+1) done: its last reader).
                     uint32_t g = ring % Cfg::kGroups;
                     w.code = kErrFwdWait + 11;
                     if (!mbar_wait(&kv_full[g], (ring / Cfg::kGroups) & 1, w)) { ok = false; break; }
@@ -305,7 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     mma_commit(&s_full[0]);
                     issue_qk<D>(tS1, q1, kaddr);
                     mma_commit(&s_full[1]);
-                    mma_commit(&kv_empty[g]);
                     for (int j = 0; j < n1; ++j) {
                         g = ring % Cfg::kGroups;
                         w.code = kErrFwdWait + 12;
@@ -338,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                             mma_commit(&o_full[1]);
                             mma_commit(q_empty);
                         }
-                        mma_commit(&kv_empty[g]);
                     }
                 } else {
                     // one query tile (D = 256): K_j and V_j in single slots,
@@ -395,6 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 20 + t};
         uint32_t sph = 0, oph = 0;
         bool ok = (t < Cfg::kNQ);
+        // With grouped K/V slots one thread of tile 1 frees each group: S1(j)
+        // complete means the MMAs of key tile j-1 (PV0, S0(j), PV1) are done
+        // too, since one thread issues them in order; O1 complete frees the
+        // unit's last group.
+        const bool releaser = Cfg::kGrouped && t == 1 && r_in_tile == 0;
+        uint32_t grp = 0;
         for (int it = 0; ok; ++it) {
             Unit un;
             if (!unit_at(it, U, BH, P, un)) break;
@@ -411,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             float l = 0.f;             // running row sum relative to m_used
             for (int j = 0; j < n; ++j) {
                 if (!mbar_wait(&s_full[t], sph, w)) { ok = false; break; }
+                if (releaser) mbar_arrive(&kv_empty[grp++ % Cfg::kGroups]);
                 sph ^= 1;
                 tc_fence_after();
                 uint32_t sr[4][32];
@@ -497,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             if (!ok) break;
             // ---- epilogue: O / l -> bf16, LSE
             if (!mbar_wait(&o_full[t], oph, w)) { ok = false; break; }
+            if (releaser) mbar_arrive(&kv_empty[grp++ % Cfg::kGroups]);
             oph ^= 1;
             tc_fence_after();
             const float inv_l = 1.f / l;

@@ -18,8 +18,8 @@
 // CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent over
 // work units):
 //   warp 0       TMA producer: Q tile pair, then K_j / V_j into a ring of
-//                shared-memory slots guarded by full/empty mbarriers (with two
-//                query tiles, one barrier pair per group of slots {V_j, K_j+1}).
+//                shared-memory slots guarded by full/empty mbarriers (at
+//                D = 128 one barrier pair per group of slots {V_j, K_j+1}).
 //   warp 1       TMEM allocator and MMA issuer (one elected lane).
 //   warps 2-3    idle (they complete warpgroup 0).
 //   warps 4-7    softmax + epilogue of query tile 0.
@@ -58,9 +58,11 @@ struct FwdCfg {
     static constexpr int kNQ = (D == 256) ? 1 : 2;
     static constexpr int kRows = kBlockM * kNQ;          // query rows per work unit
     static constexpr int kStages = (D == 64) ? 8 : (D == 128 ? 4 : 2);  // ring slots
-    // With two query tiles the slots are used in groups of two, {V_j, K_j+1},
-    // each group with one full and one empty barrier (kv_full/kv_empty[g]).
-    static constexpr bool kGrouped = (kNQ == 2);
+    // At D = 128 the slots are used in groups of two, {V_j, K_j+1}, each group
+    // with one full and one empty barrier (kv_full/kv_empty[g]): fewer waits
+    // and commits for the MMA thread.  At D = 64 the softmax, not the MMA
+    // issue, sets the pace, and single slots measured faster.
+    static constexpr bool kGrouped = (D == 128);
     static constexpr int kGroups = kStages / 2;
     static constexpr int kQBytes = kNQ * kTileBytes;
     static constexpr int kRingOff = kQBytes;
@@ -340,8 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         }
                     }
                 } else {
-                    // one query tile (D = 256): K_j and V_j in single slots,
-                    // per key tile PV(j), then S(j+1)
+                    // K_j and V_j in single slots, each with its own barriers
                     const uint32_t kslot = ring % Cfg::kStages;
                     w.code = kErrFwdWait + 11;
                     if (!mbar_wait(&kv_full[kslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
@@ -349,29 +350,64 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     tc_fence_after();
                     issue_qk<D>(tS0, q0, ring_base + kslot * Cfg::kTileBytes);
                     mma_commit(&s_full[0]);
+                    if constexpr (Cfg::kNQ == 2) {
+                        issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
+                        mma_commit(&s_full[1]);
+                    }
                     mma_commit(&kv_empty[kslot]);
-                    for (int j = 0; j < n0; ++j) {
+                    for (int j = 0; j < n1; ++j) {
                         const uint32_t vslot = ring % Cfg::kStages;
                         w.code = kErrFwdWait + 12;
                         if (!mbar_wait(&kv_full[vslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
                         ++ring;
-                        w.code = kErrFwdWait + 13;
-                        if (!mbar_wait(&p_full[0], pph0, w)) { ok = false; break; }
-                        pph0 ^= 1;
-                        tc_fence_after();
-                        issue_pv<D>(tO0, tS0, ring_base + vslot * Cfg::kTileBytes, j > 0);
-                        mma_commit(&kv_empty[vslot]);
-                        if (j + 1 < n0) {
-                            const uint32_t nslot = ring % Cfg::kStages;
-                            w.code = kErrFwdWait + 14;
-                            if (!mbar_wait(&kv_full[nslot], (ring / Cfg::kStages) & 1, w)) { ok = false; break; }
+                        const bool has_next = (j + 1 < n1);
+                        uint32_t nslot = 0, nphase = 0;
+                        if (has_next) {
+                            nslot = ring % Cfg::kStages;
+                            nphase = (ring / Cfg::kStages) & 1;
                             ++ring;
+                        }
+                        const uint32_t vaddr = ring_base + vslot * Cfg::kTileBytes;
+                        const uint32_t naddr = ring_base + nslot * Cfg::kTileBytes;
+                        bool next_ready = false;
+                        if (j < n0) {
+                            w.code = kErrFwdWait + 13;
+                            if (!mbar_wait(&p_full[0], pph0, w)) { ok = false; break; }
+                            pph0 ^= 1;
                             tc_fence_after();
-                            issue_qk<D>(tS0, q0, ring_base + nslot * Cfg::kTileBytes);
-                            mma_commit(&s_full[0]);
+                            issue_pv<D>(tO0, tS0, vaddr, j > 0);
+                            if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[vslot]);
+                            if (j + 1 < n0) {
+                                w.code = kErrFwdWait + 14;
+                                if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
+                                next_ready = true;
+                                tc_fence_after();
+                                issue_qk<D>(tS0, q0, naddr);
+                                mma_commit(&s_full[0]);
+                                if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[nslot]);
+                            } else {
+                                mma_commit(&o_full[0]);
+                                if constexpr (Cfg::kNQ == 1) mma_commit(q_empty);
+                            }
+                        }
+                        if constexpr (Cfg::kNQ == 1) continue;
+                        w.code = kErrFwdWait + 15;
+                        if (!mbar_wait(&p_full[1], pph1, w)) { ok = false; break; }
+                        pph1 ^= 1;
+                        tc_fence_after();
+                        issue_pv<D>(tO1, tS1, vaddr, j > 0);
+                        mma_commit(&kv_empty[vslot]);
+                        if (has_next) {
+                            if (!next_ready) {
+                                w.code = kErrFwdWait + 16;
+                                if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
+                                tc_fence_after();
+                            }
+                            issue_qk<D>(tS1, q1, naddr);
+                            mma_commit(&s_full[1]);
                             mma_commit(&kv_empty[nslot]);
                         } else {
-                            mma_commit(&o_full[0]);
+                            mma_commit(&o_full[1]);
                             mma_commit(q_empty);
                         }
                     }

@@ -204,6 +204,19 @@ __device__ __forceinline__ void issue_dq(uint32_t tD, uint32_t ds_saddr, uint32_
                kk > 0 ? 1u : 0u);
 }
 
+// dK (+)= dS^T Q with dS^T read from the shared copy the dQ MMA uses: rows =
+// keys, queries contiguous in two 64-query boxes, i.e. K-major A (like K in
+// S^T); B = Q (queries x D, MN-major)
+template <int D>
+__device__ __forceinline__ void issue_dk(uint32_t tAcc, uint32_t ds_saddr, uint32_t q_saddr, bool acc) {
+    const uint64_t ad = sdesc_sw128(ds_saddr, 16, 1024), bd = sdesc_sw128(q_saddr, kBox, 1024);
+#pragma unroll
+    for (int kk = 0; kk < kBlk / 16; ++kk) {
+        const uint32_t aoff16 = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+        mma_ss(tAcc, ad + aoff16, bd + ((kk * 2048) >> 4), BwdCfg<D>::kIdescAcc,
+               (acc || kk > 0) ? 1u : 0u);
+    }
+}
 
 // ---------------------------------------------------------------- main kernel
 
@@ -457,10 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     if (!ok) break;
                     ph_ds ^= 1;
                     tc_fence_after();
-                    issue_acc<D>(tdK, tY, sbase + Cfg::kOffQ + st * Cfg::kTile, !first);
-                    mma_commit(&q_empty[st]);
+                    // dQ first, so that its drain overlaps the dK MMAs; dK reads
+                    // dS from shared memory, which leaves Y to dQ
                     issue_dq<D>(tY, aDS, aK);
                     mma_commit(dq_full);
+                    issue_dk<D>(tdK, aDS, sbase + Cfg::kOffQ + st * Cfg::kTile, !first);
+                    mma_commit(&q_empty[st]);
                     if (has_next) {
                         FA_WAIT(dq_empty, ph_dqe, 18);
                         if (!ok) break;
@@ -551,9 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 w.code = kErrBwdWait + 32;
                 if (!mbar_wait(dp_full, n & 1, w)) { ok = false; break; }
                 if (n > 0) {
-                    // the dQ MMA of the previous block has finished reading dS
+                    // the dQ and dK MMAs of the previous block have finished
+                    // reading dS (dK, the later one, is committed with Q's stage)
                     w.code = kErrBwdWait + 33;
-                    if (!mbar_wait(dq_full, (n - 1) & 1, w)) { ok = false; break; }
+                    if (!mbar_wait(&q_empty[(n - 1) & 1], ((n - 1) >> 1) & 1, w)) { ok = false; break; }
                 }
                 tc_fence_after();
 #pragma unroll
@@ -574,7 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         dsw[e / 2] = mul_bf16x2(pk[(c * 32 + e) >> 1],
                                                 pack_bf16x2(__uint_as_float(dr[e]),
                                                             __uint_as_float(dr[e + 1])));
-                    tmem_st16(tY + c * 16, dsw);
                     // shared copy for the dQ MMA: queries [32c, 32c+32) of this key row,
                     // 128B-swizzled, two 64-query blocks of 16 KB
                     uint8_t *blk = ds_row + (c >> 1) * kBox;
@@ -587,7 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                   }
                 }
                 fence_proxy_async_smem();
-                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(ds_ready);
             }

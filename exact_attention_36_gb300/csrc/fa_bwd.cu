@@ -17,22 +17,25 @@
 // Main kernel: persistent, one CTA per SM, a work unit is (b, h, key tile j
 // of 128 keys).  K_j and V_j stay in shared memory; 128-query blocks Q_i,
 // dO_i stream through.  Everything is computed transposed (keys on the 128
-// TMEM lanes), so P^T and dS^T land in Tensor Memory exactly where the dV
-// and dK MMAs want their A operand:
+// TMEM lanes), so P^T lands in Tensor Memory exactly where the dV MMA wants
+// its A operand, and dS^T in shared memory in the K-major layout of dK's A:
 //   S^T  = K_j Q_i^T - LSE/scale   -> X (fp32, 128 cols)  A=K smem, B=Q smem
 //   dP^T = V_j dO_i^T - Delta      -> Y (fp32, 128 cols)  A=V smem, B=dO smem
-//   P^T = 2^(X scale log2 e) (bf16) over X;  dS^T = P^T o Y (bf16) over Y and
-//   into shared memory
+//   P^T = 2^(X scale log2 e) (bf16) over X;  dS^T = P^T o Y (bf16) into
+//   shared memory
 // The per-query terms -LSE/scale and -Delta enter through one extra K step
 // of those two MMAs: A = ones, B = the value as three bf16 terms (exact sum),
 // written by the producer next to Q_i and dO_i.  The softmax warps then read
 // no per-query statistics from shared memory, whose bandwidth the MMAs need.
 //   dV  += P^T dO_i       (TMEM acc, D cols)         A=X tmem,  B=dO smem
-//   dK  += dS^T Q_i       (TMEM acc, D cols)         A=Y tmem,  B=Q smem
 //   dQ_i = dS K_j  -> Y   (fp32, queries on lanes)   A=dS smem, B=K smem
+//   dK  += dS^T Q_i       (TMEM acc, D cols)         A=dS smem, B=Q smem
+// dQ is issued before dK so that the drain of dQ_i out of Y runs while the
+// tensor core does dK_i; dP^T(i+1) needs Y back.  (With dS^T in TMEM, dK
+// would have to read it from Y before dQ could overwrite it.)
 // Tensor Memory: X [0,128) | Y [128,256) | dV [256,256+D) | dK [256+D,256+2D).
 // tcgen05.mma from one thread executes in issue order: S(i+1) may overwrite
-// X once dV(i) was issued, dQ(i) may overwrite Y once dK(i) was issued.
+// X once dV(i) was issued, dQ(i) may overwrite Y once dS(i) was formed.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer (K_j/V_j per unit; Q_i + LSE bias rows, dO_i +

@@ -349,7 +349,7 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
         return FA_ERR_INVALID_ARG;
     if (pair_mode < -1 || pair_mode > 1) return FA_ERR_INVALID_ARG;
     // packed batches: the single-CTA kernel (D = 64, 128), atomic-order dQ
-    if (cu && (D == 256 || sem || pair_mode == 1)) return FA_ERR_UNSUPPORTED;
+    if (cu && (sem || pair_mode == 1)) return FA_ERR_UNSUPPORTED;
     // CTA pairs: D = 128 with atomic-order dQ only.  Not the default: on
     // GB300 the single-CTA kernel is faster (the pair's dQ MMA, M = 128 over
     // two SMs, runs at half the per-SM tensor rate, and the dS exchange adds

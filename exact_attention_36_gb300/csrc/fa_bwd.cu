@@ -894,15 +894,20 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
         case 64: return launch_bwd_d<64>(a, stream);
         case 128: return launch_bwd_d<128>(a, stream);
         case 256: {
-            // no ordered dQ and no packed batches at D = 256 yet
-            if (a.dq_sem || a.cu_seqlens) return cudaErrorNotSupported;
-            const long long rows = static_cast<long long>(a.B) * a.H * a.S;
+            // no ordered dQ at D = 256 yet
+            if (a.dq_sem) return cudaErrorNotSupported;
+            BwdArgs rows_view = a;  // per-token view for prep and convert, as above
+            if (a.cu_seqlens) {
+                rows_view.B = 1;
+                rows_view.S = a.T;
+            }
+            const long long rows = static_cast<long long>(rows_view.B) * a.H * rows_view.S;
             const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
-            fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(a);
+            fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(rows_view);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return e;
             if ((e = launch_bwd_main_d256(a, stream)) != cudaSuccess) return e;
-            fa_bwd_dq_cvt<256><<<blocks, 256, 0, stream>>>(a);
+            fa_bwd_dq_cvt<256><<<blocks, 256, 0, stream>>>(rows_view);
             return cudaGetLastError();
         }
         default: return cudaErrorNotSupported;

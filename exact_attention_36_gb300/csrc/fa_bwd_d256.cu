@@ -95,8 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
     const int lane = threadIdx.x & 31;
     const int H = args.H, S = args.S;
     const int BH = args.B * H;
-    const int nT = (S + kKeys - 1) / kKeys;  // key tiles
-    const int nQ = (S + kQB - 1) / kQB;      // query blocks
+    const int nT = (S + kKeys - 1) / kKeys;  // key tiles (S: the longest sequence if packed)
     const int U = BH * nT * 2;
 
     if (threadIdx.x == 0) {
@@ -141,6 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
             if (!unit256_at(it, U, nT, un)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
+            if (!sp.ok && un.j == 0 && h == 0 && un.oh == 0 && lane == 0)
+                atomicCAS(args.err_word, 0, kErrSeqlens);
+            if (un.j * kKeys >= sp.len) continue;  // past this sequence's end
+            const int nQ = (sp.len + kQB - 1) / kQB;
             if (lane == 0) {
                 w.code = kErrBwdWait + 0x51;
                 ok = mbar_wait(kv_empty, (nunit & 1) ^ 1, w);
@@ -148,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     mbar_arrive_expect_tx(kv_full, 8 * kBoxK);
                     for (int c = 0; c < 4; ++c) {
                         tma_load_4d(smem + Cfg::kOffK + c * kBoxK, &args.tm_k, kv_full, 64 * c, h,
-                                    un.j * kKeys, b);
+                                    sp.trow0 + un.j * kKeys, sp.tb);
                         tma_load_4d(smem + Cfg::kOffV + c * kBoxK, &args.tm_v, kv_full, 64 * c, h,
-                                    un.j * kKeys, b);
+                                    sp.trow0 + un.j * kKeys, sp.tb);
                     }
                 }
             }
@@ -165,15 +169,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     mbar_arrive_expect_tx(q_full, 4 * kBoxQ);
                     for (int c = 0; c < 4; ++c)
                         tma_load_4d(smem + Cfg::kOffQ + c * kBoxQ, &args.tm_q, q_full, 64 * c, h,
-                                    i * kQB, b);
+                                    sp.trow0 + i * kQB, sp.tb);
                 }
-                const size_t rbase = static_cast<size_t>(un.bh) * S;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int qr = r * 32 + lane;
                     const int q = i * kQB + qr;
-                    stat[qr] = q < S ? args.lse[rbase + q] * log2e : INFINITY;
-                    stat[64 + qr] = q < S ? args.delta[rbase + q] : 0.f;
+                    const size_t x = stat_index(args.cu_seqlens, args.T, S, H, b, h, sp, q);
+                    stat[qr] = q < sp.len ? args.lse[x] * log2e : INFINITY;
+                    stat[64 + qr] = q < sp.len ? args.delta[x] : 0.f;
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                         mbar_arrive_expect_tx(do_full, 4 * kBoxQ);
                         for (int c = 0; c < 4; ++c)
                             tma_load_4d(smem + Cfg::kOffDO + c * kBoxQ, &args.tm_do, do_full,
-                                        64 * c, h, i * kQB, b);
+                                        64 * c, h, sp.trow0 + i * kQB, sp.tb);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -217,6 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                 Unit256 un;
                 if (!unit256_at(it, U, nT, un)) break;
                 if (un.j < 0) continue;
+                const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
+                if (un.j * kKeys >= sp.len) continue;
+                const int nQ = (sp.len + kQB - 1) / kQB;
                 FA_WAIT(kv_full, nunit & 1, 0x60);
                 if (!ok) break;
                 const int i0 = first_qblock(un.j);
@@ -301,6 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
             Unit256 un;
             if (!unit256_at(it, U, nT, un)) break;
             if (un.j < 0) continue;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
+            if (un.j * kKeys >= sp.len) continue;
+            const int nQ = (sp.len + kQB - 1) / kQB;
             const int key = un.j * kKeys + kr;
             for (int i = first_qblock(un.j); i < nQ; ++i, ++n) {
                 w.code = kErrBwdWait + 0x70;
@@ -316,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     tmem_ld_wait(sr[0]);
                     tmem_ld_wait(sr[1]);
                     const bool diag = args.causal && (i * kQB < (un.j + 1) * kKeys);
-                    if (diag || (un.j + 1) * kKeys > S) {
-                        const bool key_ok = key < S;
+                    if (diag || (un.j + 1) * kKeys > sp.len) {
+                        const bool key_ok = key < sp.len;
                         const int q0 = i * kQB;
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
@@ -397,6 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
             if (!unit256_at(it, U, nT, un)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
+            const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
+            if (un.j * kKeys >= sp.len) continue;
+            const int nQ = (sp.len + kQB - 1) / kQB;
+            // accumulator rows: [B*H, S] fixed, [H, T] packed
+            const int acc_row0 = args.cu_seqlens ? sp.tok0 : 0;
+            const int acc_z = args.cu_seqlens ? h : un.bh;
             for (int i = first_qblock(un.j); i < nQ; ++i, ++n) {
                 w.code = kErrBwdWait + 0x80;
                 if (!mbar_wait(dq_full, n & 1, w)) { ok = false; break; }
@@ -420,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     __syncwarp();
                     if (lane == 0) {
                         tma_reduce_add_3d(&args.tm_dqacc, stage, un.oh * 128 + quarter * 32,
-                                          i * kQB + half * 32, un.bh);
+                                          acc_row0 + i * kQB + half * 32, acc_z);
                         bulk_commit();
                     }
                 }
@@ -431,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
             ++nunit;
             tc_fence_after();
             const int key = un.j * kKeys + r;  // dK / dV lanes are keys
-            const size_t orow = ((static_cast<size_t>(b) * S + key) * H + h) * kD + un.oh * 128;
+            const size_t orow = ((static_cast<size_t>(sp.tok0) + key) * H + h) * kD + un.oh * 128;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
@@ -447,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
                                             __uint_as_float(v[2 * e + 1]) * mul);
-                    if (key < S) {
+                    if (key < sp.len) {
                         uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4)

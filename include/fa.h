@@ -139,9 +139,8 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
  * dv bf16 [total, H, D]; lse fp32 [H, total] from fa_fwd_varlen; dq_acc fp32
  * [H, total, D] and delta fp32 [H, total] scratch, fa_bwd_varlen_workspace_size
  * bytes in all (carved like fa_bwd's).  cu_seqlens and max_seqlen as for the
- * forward, with the same 0x300 report for bad offsets.  D = 64 and 128;
- * D = 256 returns FA_ERR_UNSUPPORTED.  Other arguments, results and errors as
- * fa_bwd.
+ * forward, with the same 0x300 report for bad offsets.  D in {64, 128, 256}.
+ * Other arguments, results and errors as fa_bwd.
  */
 size_t fa_bwd_varlen_workspace_size(int total, int H, int D);
 fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,

@@ -106,7 +106,7 @@ def _check_bwd_each(q, k, v, do, cu, dq, dk, dv, causal, scale):
                        dk[None, sl], dv[None, sl], causal, scale, heads=None)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_ragged_mix(D, causal):
     lengths = [1, 127, 128, 129, 300, 2, 640, 257]
@@ -138,9 +138,22 @@ def test_backward_matches_fixed_length_kernel():
     assert ((dq.view(shp).float() - dq2.float()).norm() / dq2.float().norm()).item() <= 1e-3
 
 
-def test_backward_rejects_what_it_does_not_cover():
-    q = torch.zeros(256, 2, 256, dtype=torch.bfloat16, device="cuda")
-    cu = torch.tensor([0, 100, 256], dtype=torch.int32, device="cuda")
-    o, lse = fa.forward_varlen(q, q, q, cu, 156)
-    with pytest.raises(fa.FAError, match="UNSUPPORTED"):
-        fa.backward_varlen(q, q, q, o, q, lse, cu, 156)
+def test_backward_d256_random_lengths_and_stress():
+    lengths = packed_lengths(6, 700, seed=8)
+    args = _bwd(lengths, 2, 256, True, seed=8, stress=True)
+    _check_bwd_each(*args[:8], True, args[8])
+
+
+def test_backward_d256_matches_fixed_length_kernel():
+    B, H, S, D = 2, 2, 300, 256
+    q, k, v, do, cu = make_packed([S] * B, H, D, seed=9)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.forward_varlen(qd, kd, vd, cu.cuda(), S, causal=False)
+    dq, dk, dv = fa.backward_varlen(qd, kd, vd, o, dod, lse, cu.cuda(), S, causal=False)
+    shp = (B, S, H, D)
+    o2, lse2 = fa.forward(qd.view(shp), kd.view(shp), vd.view(shp), causal=False)
+    dq2, dk2, dv2 = fa.backward(qd.view(shp), kd.view(shp), vd.view(shp), o2, dod.view(shp), lse2,
+                                causal=False)
+    torch.cuda.synchronize()
+    assert torch.equal(dk.view(shp), dk2) and torch.equal(dv.view(shp), dv2)
+    assert ((dq.view(shp).float() - dq2.float()).norm() / dq2.float().norm()).item() <= 1e-3

@@ -139,6 +139,13 @@ fa_status check_shape(int B, int H, int S, int D, float scale) {
     return FA_OK;
 }
 
+// Deterministic-mode scratch: counters [B*H][ceil(S/64)], then the order keys
+// [B*H][ceil(S/128)] of the key tiles; each part padded to 256 bytes.
+size_t sem_counter_bytes(int B, int H, int S) {
+    const size_t n = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 63) / 64);
+    return (n * sizeof(int) + 255) & ~static_cast<size_t>(255);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kDefaultRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 between rescales
 // Measured on GB300 (S = 32768, D = 128): 0 of 8 columns on the FMA
@@ -382,6 +389,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     a.dq_acc = dq_acc;
     a.delta = delta;
     a.dq_sem = sem;
+    a.dq_key = sem ? reinterpret_cast<int *>(reinterpret_cast<char *>(sem) + sem_counter_bytes(B, H, S))
+                   : nullptr;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -435,8 +444,8 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
 
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D) {
     if (check_shape(B, H, S, D, 1.f) != FA_OK) return 0;
-    const size_t n = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 63) / 64);
-    return (n * sizeof(int) + 255) & ~static_cast<size_t>(255);
+    const size_t u = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 127) / 128);
+    return sem_counter_bytes(B, H, S) + ((u * sizeof(int) + 255) & ~static_cast<size_t>(255));
 }
 
 fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,

@@ -130,24 +130,62 @@ __device__ __forceinline__ int block_at(int j, int s, int i0, int nb, bool rotat
     return rotate ? (j + s) % nb : i0 + s;
 }
 
-// Fixed-order mode: the place of key tile j's contribution in the sum of dQ
-// block i (0 = first).  Units are numbered head by head (unit u = bh nT + j)
-// and taken in rounds of G by the persistent grid; [j0, j1) are the head's
-// tiles in j's round.  Contributions of earlier rounds come first; within a
-// round they are ordered by the step at which each tile reaches block i, so
-// every wait points to a unit of the same round or an earlier one (no cycle),
-// and in the same round to the tile one step ahead.
-__device__ __forceinline__ int dq_position(int bh, int j, int i, int nT, int G, bool causal) {
+// Fixed-order mode without a causal mask: the place of key tile j's
+// contribution in the sum of dQ block i (0 = first).  Units are numbered head
+// by head (unit u = bh nT + j) and taken in rounds of G by the persistent
+// grid; [j0, j1) are the head's tiles in j's round.  Contributions of earlier
+// rounds come first; within a round they are ordered by the step at which
+// each tile reaches block i, so every wait points to a unit of the same round
+// or an earlier one (no cycle), and in the same round to the tile one step
+// ahead.
+__device__ __forceinline__ int dq_position(int bh, int j, int i, int nT, int G) {
     const int r = (bh * nT + j) / G;
     const int j0 = max(r * G - bh * nT, 0), j1 = min((r + 1) * G - bh * nT, nT);
-    if (causal)  // tiles j' <= i, reached at step i - j'
-        return min(i + 1, j0) + (min(i, j1 - 1) - j);
     // every tile sees every block, reached at step (i - j') mod nT: earlier
     // steps are the tiles in the circular range (j, i]
     auto in_round = [&](int lo, int hi) { return max(0, min(j1, hi) - max(j0, lo)); };
     const int ahead = j < i ? in_round(j + 1, i + 1)
                             : (j > i ? in_round(j + 1, nT) + in_round(0, i + 1) : 0);
     return j0 + ahead;
+}
+
+// Fixed-order mode under a causal mask.  Tile lengths differ (tile j visits
+// blocks j .. nT-1), so a CTA starts its next unit whenever its current one
+// ends, and a fixed order by rounds would make the CTAs that move on early
+// wait for the longest tiles.  Instead the order follows the schedule itself:
+// counting one step per block, tile j of unit u starts at step start(u) (the
+// lengths of the units its CTA ran before, in the persistent grid's
+// serpentine order) and reaches block i at step start(u) + i - j.  The
+// contributions to block i are summed in the order of that arrival step
+// (ties: lower j first), i.e. by key(u) = start(u) - j.  Along one CTA's
+// sequence of blocks the arrival step strictly increases, and every wait
+// points to a strictly earlier (step, tile), so the waits form no cycle.
+__device__ __forceinline__ int causal_order_key(int u, int U, int nT, int G) {
+    const int r = u / G, p = u % G;
+    const int c = (r & 1) ? G - 1 - p : p;  // the CTA that runs unit u
+    long long start = 0;
+    for (int rr = 0; rr < r; ++rr) {
+        const int uu = rr * G + ((rr & 1) ? G - 1 - c : c);
+        if (uu < U) start += nT - uu % nT;
+    }
+    return static_cast<int>(start - u % nT);
+}
+
+// Rank of tile j among the tiles j' <= i of its head by (key, j'): its place
+// in the sum of dQ block i.  All lanes of the warp take part.
+__device__ __forceinline__ int causal_rank(const int *keys, int j, int i, int lane) {
+    const int kj = keys[j];
+    int cnt = 0;
+    for (int base = 0; base <= i; base += 32) {
+        const int jp = base + lane;
+        bool before = false;
+        if (jp <= i) {
+            const int kp = keys[jp];
+            before = kp < kj || (kp == kj && jp < j);
+        }
+        cnt += __popc(__ballot_sync(0xffffffffu, before));
+    }
+    return cnt;
 }
 
 // ---------------------------------------------------------------- MMA helpers
@@ -701,11 +739,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         sem_prev = nullptr;
                     }
                     int *sem = args.dq_sem + static_cast<size_t>(un.bh) * nSem + (i * kBlk) / 64;
+                    const int place =
+                        args.causal ? causal_rank(args.dq_key + static_cast<size_t>(un.bh) * nT, un.j, i, lane)
+                                    : dq_position(un.bh, un.j, i, nT, gridDim.x);
                     bool go = true;
                     if (lane == 0) {
                         w.code = kErrBwdWait + 42;
-                        go = counter_wait_geq(
-                            sem, dq_position(un.bh, un.j, i, nT, gridDim.x, args.causal != 0), w);
+                        go = counter_wait_geq(sem, place, w);
                         fence_proxy_async_global();
                     }
                     go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
@@ -794,6 +834,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
 // the dQ accumulator set to zero.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdArgs args) {
+    if (args.dq_key && args.causal) {
+        // fixed-order mode: the order key of every unit (causal_order_key)
+        const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+        const int nT = (args.S + kBlk - 1) / kBlk;
+        const long long U = static_cast<long long>(args.B) * args.H * nT;
+        if (t < U) args.dq_key[t] = causal_order_key(static_cast<int>(t), static_cast<int>(U), nT, args.grid);
+    }
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const long long rows = static_cast<long long>(args.B) * args.H * args.S;
@@ -852,7 +899,10 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     using Cfg = BwdCfg<D>;
     // Delta, the accumulator and dQ are per token: the prep and convert
     // kernels see a packed batch as one sequence of T tokens
+    const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
+    const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
     BwdArgs rows_view = a;
+    rows_view.grid = grid;
     if (a.cu_seqlens) {
         rows_view.B = 1;
         rows_view.S = a.T;
@@ -870,8 +920,6 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     auto kern = a.dq_sem ? fa_bwd_kernel<D, true> : fa_bwd_kernel<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
-    const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
     if (a.dq_sem) {
         // CTAs wait on one another's dQ counters: a cooperative launch
         // guarantees they are all resident at once

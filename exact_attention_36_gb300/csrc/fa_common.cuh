@@ -41,6 +41,8 @@ struct BwdArgs {
     float *dq_acc;                        // fp32 [B,H,S,D]
     float *delta;                         // fp32 [B,H,S]
     int *dq_sem;                          // deterministic mode: [B*H][ceil(S/64)] counters, else null
+    int *dq_key;                          // deterministic mode: [B*H][ceil(S/128)] order keys of the key tiles
+    int grid;                             // main kernel's persistent grid (for the order keys)
     void *dq, *dk, *dv;                   // bf16 [B,S,H,D]
     int B, H, S, D;
     int causal;

@@ -177,12 +177,15 @@ fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
  * over the key tiles in an order fixed by (B, H, S, causal) and the device's
  * SM count, so repeated calls on the same inputs on the same GPU model give
  * bitwise-identical dQ, dK and dV.  Each 128-query block has a counter; the
- * key tile whose turn it is adds its share, and the order puts the tiles that
- * run at the same time one step apart, so few of them wait.  The kernel is
+ * key tile whose turn it is adds its share.  Without a causal mask the order
+ * puts the tiles that run at the same time one step apart; with one, the
+ * tiles are taken in the order they reach the block in the persistent
+ * schedule (one step per block), so few of them wait.  The kernel is
  * launched cooperatively, so all its CTAs are resident while they wait on one
  * another.
- *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes (contents on
- *            entry ignored; the first launch zeroes it).
+ *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes: the
+ *            counters, then the order keys of the key tiles (contents on
+ *            entry ignored; the first launch writes both).
  * Other arguments, results and errors as fa_bwd.  D = 256 returns
  * FA_ERR_UNSUPPORTED.
  */

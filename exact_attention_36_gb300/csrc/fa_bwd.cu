@@ -752,33 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, go);
                     sem_prev = sem;
                 } else {
-                    // Atomic order.  This instance is launched only without
-                    // dq_sem, so the sem branches below never run; they are kept
-                    // because ptxas allocates the kernel's registers differently
-                    // without them (36 instead of 4 bytes of spills), which
-                    // measured 2-3 % slower on GB300 (same-box A/B).
-                    int *sem = args.dq_sem ? args.dq_sem + static_cast<size_t>(un.bh) * nSem +
-                                                 (i * kBlk) / 64
-                                           : nullptr;
-                    bool go = true;
-                    if (sem) {
-                        if (lane == 0) {
-                            w.code = kErrBwdWait + 42;
-                            go = counter_wait_geq(sem, un.j, w);
-                            fence_proxy_async_global();
-                        }
-                        go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-                    }
-                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, go);
-                    if (sem) {
-                        if (lane == 0) {
-                            bulk_wait<0>();
-                            fence_proxy_async_global();
-                            __threadfence();
-                        }
-                        named_bar_sync(1, 128);
-                        if (leader) red_release_gpu_add(sem, 1);
-                    }
+                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, true);
                 }
             }
             if (kDet && sem_prev) {  // the unit's last block

@@ -1,6 +1,6 @@
 """Pins for the fp64 CPU oracle (no GPU).
 
-The oracle is the judge of the CUDA kernels, so it is itself checked against
+The CUDA kernels are checked against the oracle, so it is itself checked against
 things that do not come from it: hand-derived closed forms (tests/golden),
 invariants of softmax attention and of its gradient, a library routine
 (torch's CPU float64 scaled_dot_product_attention and autograd), and central

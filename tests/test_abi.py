@@ -93,6 +93,20 @@ def test_workspace_size(lib):
     assert lib.fa_bwd_workspace_size(B, H, S, 96) == 0
 
 
+def test_semaphore_and_varlen_scratch_sizes(lib):
+    # fixed-order mode: counters per 64 query rows, then one order key per
+    # 128-key tile, each part padded to 256 bytes
+    B, H, S, D = 2, 3, 1000, 128
+    counters = B * H * ((S + 63) // 64)
+    keys = B * H * ((S + 127) // 128)
+    want = (counters * 4 + 255) // 256 * 256 + (keys * 4 + 255) // 256 * 256
+    assert lib.fa_bwd_semaphore_bytes(B, H, S, D) == want
+    assert lib.fa_bwd_semaphore_bytes(B, H, 0, D) == 0
+    # packed batches: the accumulator and Delta over all tokens, as fa_bwd's
+    T = 1234
+    assert lib.fa_bwd_varlen_workspace_size(T, H, D) == lib.fa_bwd_workspace_size(1, H, T, D)
+
+
 def _coeffs(deg):
     text = open(COEFFS).read()
     return [float(re.search(rf"FA_EXP2_P{deg}_C{i} ([-+0-9.e]+)f", text).group(1))

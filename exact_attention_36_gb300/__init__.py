@@ -9,7 +9,9 @@ Importing this package is cheap; the library is loaded on first use of
 ``forward`` / ``backward`` (and the other names re-exported from ``fa``).
 """
 
-__all__ = ["forward", "backward", "fwd", "bwd", "bwd_workspace_size", "FAError"]
+__all__ = ["forward", "backward", "forward_varlen", "backward_varlen", "fwd", "bwd",
+           "bwd_deterministic", "fwd_varlen", "bwd_varlen", "bwd_workspace_size",
+           "bwd_semaphore_bytes", "FAError"]
 
 
 def __getattr__(name):

@@ -389,7 +389,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     a.dq_acc = dq_acc;
     a.delta = delta;
     a.dq_sem = sem;
-    a.dq_key = sem ? reinterpret_cast<int *>(reinterpret_cast<char *>(sem) + sem_counter_bytes(B, H, S))
+    a.dq_key = (sem && D != 256)
+                   ? reinterpret_cast<int *>(reinterpret_cast<char *>(sem) + sem_counter_bytes(B, H, S))
                    : nullptr;
     a.dq = dq;
     a.dk = dk;
@@ -444,6 +445,7 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
 
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D) {
     if (check_shape(B, H, S, D, 1.f) != FA_OK) return 0;
+    if (D == 256) return 2 * sem_counter_bytes(B, H, S);  // one counter set per output half
     const size_t u = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 127) / 128);
     return sem_counter_bytes(B, H, S) + ((u * sizeof(int) + 255) & ~static_cast<size_t>(255));
 }

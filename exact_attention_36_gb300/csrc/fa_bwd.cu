@@ -839,8 +839,14 @@ __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdAr
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
         args.delta[row] = acc;
-        if (args.dq_sem && (q & 63) == 0)
-            args.dq_sem[bh * ((S + 63) / 64) + q / 64] = 0;
+        if (args.dq_sem && (q & 63) == 0) {
+            if constexpr (D == 256) {  // one counter per (head, output half, 64 rows)
+                args.dq_sem[(bh * 2) * ((S + 63) / 64) + q / 64] = 0;
+                args.dq_sem[(bh * 2 + 1) * ((S + 63) / 64) + q / 64] = 0;
+            } else {
+                args.dq_sem[bh * ((S + 63) / 64) + q / 64] = 0;
+            }
+        }
     }
     float4 *z = reinterpret_cast<float4 *>(args.dq_acc + static_cast<size_t>(row) * D);
 #pragma unroll
@@ -916,8 +922,6 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
         case 64: return launch_bwd_d<64>(a, stream);
         case 128: return launch_bwd_d<128>(a, stream);
         case 256: {
-            // no ordered dQ at D = 256 yet
-            if (a.dq_sem) return cudaErrorNotSupported;
             BwdArgs rows_view = a;  // per-token view for prep and convert, as above
             if (a.cu_seqlens) {
                 rows_view.B = 1;

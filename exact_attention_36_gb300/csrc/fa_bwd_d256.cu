@@ -40,7 +40,7 @@ struct Cfg {
     static constexpr int kOffRed = kOffDS + 16384;    // 2 x (64 rows x 32 fp32) dQ staging
     static constexpr int kOffStat = kOffRed + 16384;  // 64 lse2 + 64 delta
     static constexpr int kOffBar = kOffStat + 512;
-    static constexpr int kNumBars = 15;
+    static constexpr int kNumBars = 16;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked)
     static constexpr uint32_t kTX = 0, kTY = 64, kTdV = 128, kTdK = 256;
@@ -71,6 +71,9 @@ __device__ __forceinline__ bool unit256_at(int it, int U, int nT, Unit256 &out) 
     return true;
 }
 
+// kDet: the fixed-order dQ mode (args.dq_sem set), a separate instance so that
+// the atomic-order kernel carries none of its logic
+template <bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_constant__ BwdArgs args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
@@ -87,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
     uint64_t *dq_full = bars + 10, *dq_empty = bars + 11;
     uint64_t *dkdv_full = bars + 12, *dkdv_empty = bars + 13;
     uint64_t *drain = bars + 14;
+    uint64_t *rel_bar = bars + 15;  // fixed-order mode: the four drain warps' reductions done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
     float *stat = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // lse2[64] | delta[64]
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
         mbar_init(dkdv_full, 1);
         mbar_init(dkdv_empty, 128);
         mbar_init(drain, 1);
+        mbar_init(rel_bar, 4);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -400,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         uint8_t *stage = smem + Cfg::kOffRed + quarter * 4096;
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x80};
-        uint32_t n = 0, nunit = 0;
+        uint32_t n = 0, nunit = 0, nrel = 0;
+        const int nQs = (S + kQB - 1) / kQB;  // fixed-order counters per head and half
         bool ok = true;
         for (int it = 0; ok; ++it) {
             Unit256 un;
@@ -424,6 +430,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                 tmem_ld_wait(col[1]);
                 tc_fence_before();
                 mbar_arrive(dq_empty);
+                // Fixed-order mode: the key tiles add their shares of this
+                // (head, half, 64-query block) in ascending order.  Units are
+                // numbered with ascending key tiles within a head and half and
+                // taken in rounds by the persistent grid, so a tile waits only
+                // for units of its own round or of earlier ones (no cycle).
+                int *sem = nullptr;
+                bool go = true;
+                if constexpr (kDet) {
+                    sem = args.dq_sem + (static_cast<size_t>(un.bh) * 2 + un.oh) * nQs + i;
+                    if (lane == 0) {
+                        w.code = kErrBwdWait + 0x82;
+                        go = counter_wait_geq(sem, un.j, w);
+                        fence_proxy_async_global();
+                    }
+                    go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+                }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     if (lane == 0) bulk_wait_read<0>();  // previous reduction has read `stage`
@@ -434,11 +456,24 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                                                    (lane & 3) * 4) = __uint_as_float(col[half][q]);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
+                    if (lane == 0 && go) {
                         tma_reduce_add_3d(&args.tm_dqacc, stage, un.oh * 128 + quarter * 32,
                                           acc_row0 + i * kQB + half * 32, acc_z);
                         bulk_commit();
                     }
+                }
+                if (kDet && sem) {
+                    // this block's share is complete in L2 in all four warps,
+                    // then the first of them passes the turn on
+                    if (lane == 0) {
+                        bulk_wait<0>();
+                        fence_proxy_async_global();
+                        __threadfence();
+                        mbar_arrive(rel_bar);
+                        w.code = kErrBwdWait + 0x83;
+                        if (mbar_wait(rel_bar, nrel & 1, w) && quarter == 0) red_release_gpu_add(sem, 1);
+                    }
+                    ++nrel;
                 }
             }
             if (!ok) break;
@@ -487,12 +522,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
 }  // namespace
 
 cudaError_t launch_bwd_main_d256(const BwdArgs &a, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel_d256,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    auto kern = a.dq_sem ? fa_bwd_kernel_d256<true> : fa_bwd_kernel_d256<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kKeys - 1) / kKeys) * 2;
     const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
-    fa_bwd_kernel_d256<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
+    if (a.dq_sem) {
+        // CTAs wait on one another's counters: all must be resident at once
+        void *params[] = {const_cast<BwdArgs *>(&a)};
+        e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid),
+                                        dim3(kThreads), params, Cfg::kSmemBytes, stream);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(a);
     return cudaGetLastError();
 }
 

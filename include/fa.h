@@ -186,8 +186,9 @@ fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
  *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes: the
  *            counters, then the order keys of the key tiles (contents on
  *            entry ignored; the first launch writes both).
- * Other arguments, results and errors as fa_bwd.  D = 256 returns
- * FA_ERR_UNSUPPORTED.
+ * At D = 256 (a work unit is a key tile and one half of the head dim) the
+ * key tiles take their turns in ascending order per half.
+ * Other arguments, results and errors as fa_bwd.
  */
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D);
 fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,

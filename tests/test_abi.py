@@ -102,6 +102,8 @@ def test_semaphore_and_varlen_scratch_sizes(lib):
     want = (counters * 4 + 255) // 256 * 256 + (keys * 4 + 255) // 256 * 256
     assert lib.fa_bwd_semaphore_bytes(B, H, S, D) == want
     assert lib.fa_bwd_semaphore_bytes(B, H, 0, D) == 0
+    # D = 256: one set of counters per half of the head dim, no order keys
+    assert lib.fa_bwd_semaphore_bytes(B, H, S, 256) == 2 * ((counters * 4 + 255) // 256 * 256)
     # packed batches: the accumulator and Delta over all tokens, as fa_bwd's
     T = 1234
     assert lib.fa_bwd_varlen_workspace_size(T, H, D) == lib.fa_bwd_workspace_size(1, H, T, D)

@@ -10,7 +10,7 @@ Importing this package is cheap; the library is loaded on first use of
 """
 
 __all__ = ["forward", "backward", "forward_varlen", "backward_varlen", "fwd", "bwd",
-           "bwd_deterministic", "fwd_varlen", "bwd_varlen", "bwd_workspace_size",
+           "bwd_deterministic", "fwd_varlen", "bwd_varlen", "bwd_varlen_deterministic", "bwd_workspace_size",
            "bwd_semaphore_bytes", "FAError"]
 
 

@@ -356,7 +356,7 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
         return FA_ERR_INVALID_ARG;
     if (pair_mode < -1 || pair_mode > 1) return FA_ERR_INVALID_ARG;
     // packed batches: the single-CTA kernel (D = 64, 128), atomic-order dQ
-    if (cu && (sem || pair_mode == 1)) return FA_ERR_UNSUPPORTED;
+    if (cu && pair_mode == 1) return FA_ERR_UNSUPPORTED;
     // CTA pairs: D = 128 with atomic-order dQ only.  Not the default: on
     // GB300 the single-CTA kernel is faster (the pair's dQ MMA, M = 128 over
     // two SMs, runs at half the per-SM tensor rate, and the dS exchange adds
@@ -440,6 +440,16 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
                         int total, int H, int D, int causal, float scale, void *stream) {
     if (!cu_seqlens) return FA_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, nullptr, dq, dk, dv, cu_seqlens, B, H,
+                    max_seqlen, total, D, causal, scale, 0, stream);
+}
+
+fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                      const void *dout, const float *lse, float *dq_acc,
+                                      float *delta, int *dq_sem, void *dq, void *dk, void *dv,
+                                      const int *cu_seqlens, int B, int max_seqlen, int total,
+                                      int H, int D, int causal, float scale, void *stream) {
+    if (!cu_seqlens || !dq_sem || !aligned16(dq_sem)) return FA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, cu_seqlens, B, H,
                     max_seqlen, total, D, causal, scale, 0, stream);
 }
 

@@ -138,14 +138,16 @@ __device__ __forceinline__ int block_at(int j, int s, int i0, int nb, bool rotat
 // each tile reaches block i, so every wait points to a unit of the same round
 // or an earlier one (no cycle), and in the same round to the tile one step
 // ahead.
-__device__ __forceinline__ int dq_position(int bh, int j, int i, int nT, int G) {
+// In a packed batch unit numbers still run over nT (the longest sequence's
+// tiles); a sequence has nb <= nT tiles, and its units past them are skipped.
+__device__ __forceinline__ int dq_position(int bh, int j, int i, int nT, int nb, int G) {
     const int r = (bh * nT + j) / G;
-    const int j0 = max(r * G - bh * nT, 0), j1 = min((r + 1) * G - bh * nT, nT);
-    // every tile sees every block, reached at step (i - j') mod nT: earlier
+    const int j0 = min(max(r * G - bh * nT, 0), nb), j1 = min((r + 1) * G - bh * nT, nb);
+    // every tile sees every block, reached at step (i - j') mod nb: earlier
     // steps are the tiles in the circular range (j, i]
     auto in_round = [&](int lo, int hi) { return max(0, min(j1, hi) - max(j0, lo)); };
     const int ahead = j < i ? in_round(j + 1, i + 1)
-                            : (j > i ? in_round(j + 1, nT) + in_round(0, i + 1) : 0);
+                            : (j > i ? in_round(j + 1, nb) + in_round(0, i + 1) : 0);
     return j0 + ahead;
 }
 
@@ -160,13 +162,21 @@ __device__ __forceinline__ int dq_position(int bh, int j, int i, int nT, int G) 
 // (ties: lower j first), i.e. by key(u) = start(u) - j.  Along one CTA's
 // sequence of blocks the arrival step strictly increases, and every wait
 // points to a strictly earlier (step, tile), so the waits form no cycle.
-__device__ __forceinline__ int causal_order_key(int u, int U, int nT, int G) {
+// Tiles of the sequence of unit u (b = u / nT / H): nT, or fewer in a packed
+// batch (0 for a sequence whose offsets are invalid).
+__device__ __forceinline__ int seq_tiles(const BwdArgs &args, int u, int nT) {
+    if (!args.cu_seqlens) return nT;
+    const SeqSpan sp = seq_span(args.cu_seqlens, args.T, args.S, (u / nT) / args.H);
+    return (sp.len + kBlk - 1) / kBlk;
+}
+
+__device__ __forceinline__ int causal_order_key(const BwdArgs &args, int u, int U, int nT, int G) {
     const int r = u / G, p = u % G;
     const int c = (r & 1) ? G - 1 - p : p;  // the CTA that runs unit u
     long long start = 0;
     for (int rr = 0; rr < r; ++rr) {
         const int uu = rr * G + ((rr & 1) ? G - 1 - c : c);
-        if (uu < U) start += nT - uu % nT;
+        if (uu < U) start += max(seq_tiles(args, uu, nT) - uu % nT, 0);  // skipped units take no steps
     }
     return static_cast<int>(start - u % nT);
 }
@@ -741,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     int *sem = args.dq_sem + static_cast<size_t>(un.bh) * nSem + (i * kBlk) / 64;
                     const int place =
                         args.causal ? causal_rank(args.dq_key + static_cast<size_t>(un.bh) * nT, un.j, i, lane)
-                                    : dq_position(un.bh, un.j, i, nT, gridDim.x);
+                                    : dq_position(un.bh, un.j, i, nT, nb, gridDim.x);
                     bool go = true;
                     if (lane == 0) {
                         w.code = kErrBwdWait + 42;
@@ -808,13 +818,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
 // the dQ accumulator set to zero.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdArgs args) {
-    if (args.dq_key && args.causal) {
-        // fixed-order mode: the order key of every unit (causal_order_key)
-        const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-        const int nT = (args.S + kBlk - 1) / kBlk;
-        const long long U = static_cast<long long>(args.B) * args.H * nT;
-        if (t < U) args.dq_key[t] = causal_order_key(static_cast<int>(t), static_cast<int>(U), nT, args.grid);
-    }
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const long long rows = static_cast<long long>(args.B) * args.H * args.S;
@@ -839,18 +842,29 @@ __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdAr
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
         args.delta[row] = acc;
-        if (args.dq_sem && (q & 63) == 0) {
-            if constexpr (D == 256) {  // one counter per (head, output half, 64 rows)
-                args.dq_sem[(bh * 2) * ((S + 63) / 64) + q / 64] = 0;
-                args.dq_sem[(bh * 2 + 1) * ((S + 63) / 64) + q / 64] = 0;
-            } else {
-                args.dq_sem[bh * ((S + 63) / 64) + q / 64] = 0;
-            }
-        }
     }
     float4 *z = reinterpret_cast<float4 *>(args.dq_acc + static_cast<size_t>(row) * D);
 #pragma unroll
     for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Fixed-order mode: zero the counters (one per (sequence, head, 64 rows) of
+// the longest sequence; at D = 256 one per output half as well) and, under a
+// causal mask at D = 64 and 128, write each unit's order key.  Launched with
+// the batch as given (not the per-token view of a packed batch).
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_det_setup(const __grid_constant__ BwdArgs args) {
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nctr = static_cast<long long>(args.B) * args.H * ((args.S + 63) / 64) * (D == 256 ? 2 : 1);
+    if (t < nctr) args.dq_sem[t] = 0;
+    if constexpr (D != 256) {
+        if (args.dq_key && args.causal) {
+            const int nT = (args.S + kBlk - 1) / kBlk;
+            const long long U = static_cast<long long>(args.B) * args.H * nT;
+            if (t < U)
+                args.dq_key[t] = causal_order_key(args, static_cast<int>(t), static_cast<int>(U), nT, args.grid);
+        }
+    }
 }
 
 // One warp per (b, h, query row): dQ[b, q, h, :] = bf16(scale * accumulator).
@@ -875,6 +889,17 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_cvt(const __grid_constant__ Bwd
 }
 
 template <int D>
+cudaError_t launch_det_setup(const BwdArgs &a, int grid, cudaStream_t stream) {
+    BwdArgs sa = a;
+    sa.grid = grid;
+    const long long nctr = static_cast<long long>(a.B) * a.H * ((a.S + 63) / 64) * (D == 256 ? 2 : 1);
+    const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
+    const long long n = nctr > U ? nctr : U;
+    fa_bwd_det_setup<D><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(sa);
+    return cudaGetLastError();
+}
+
+template <int D>
 cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     using Cfg = BwdCfg<D>;
     // Delta, the accumulator and dQ are per token: the prep and convert
@@ -882,15 +907,16 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
     const int grid = static_cast<int>(U < a.num_sms ? U : a.num_sms);
     BwdArgs rows_view = a;
-    rows_view.grid = grid;
     if (a.cu_seqlens) {
         rows_view.B = 1;
         rows_view.S = a.T;
     }
     const long long rows = static_cast<long long>(rows_view.B) * a.H * rows_view.S;
     const long long blocks = (rows * 32 + 255) / 256;
+    cudaError_t e;
+    if (a.dq_sem && (e = launch_det_setup<D>(a, grid, stream)) != cudaSuccess) return e;
     fa_bwd_prep<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(rows_view);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.pair) {
         if ((e = launch_bwd_main_pair(a, stream)) != cudaSuccess) return e;
@@ -929,8 +955,10 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
             }
             const long long rows = static_cast<long long>(rows_view.B) * a.H * rows_view.S;
             const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+            cudaError_t e;
+            if (a.dq_sem && (e = launch_det_setup<256>(a, 0, stream)) != cudaSuccess) return e;
             fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(rows_view);
-            cudaError_t e = cudaGetLastError();
+            e = cudaGetLastError();
             if (e != cudaSuccess) return e;
             if ((e = launch_bwd_main_d256(a, stream)) != cudaSuccess) return e;
             fa_bwd_dq_cvt<256><<<blocks, 256, 0, stream>>>(rows_view);

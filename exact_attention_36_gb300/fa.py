@@ -56,6 +56,7 @@ def lib():
         L.fa_bwd_varlen_workspace_size.argtypes = [i, i, i]
         L.fa_bwd_varlen_workspace_size.restype = ctypes.c_size_t
         L.fa_bwd_deterministic.argtypes = [vp] * 12 + [i, i, i, i, i, f, vp]
+        L.fa_bwd_varlen_deterministic.argtypes = [vp] * 13 + [i, i, i, i, i, i, f, vp]
         L.fa_bwd_semaphore_bytes.argtypes = [i, i, i, i]
         L.fa_bwd_semaphore_bytes.restype = ctypes.c_size_t
         L.fa_status_string.argtypes = [i]
@@ -65,7 +66,7 @@ def lib():
         L.fa_exp2_eval.argtypes = [vp, vp, ll, i, vp]
         L.fa_exp2_sweep.argtypes = [f, f, i, vp, vp]
         for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_bwd", "fa_bwd_ex", "fa_bwd_varlen",
-                     "fa_bwd_deterministic",
+                     "fa_bwd_deterministic", "fa_bwd_varlen_deterministic",
                      "fa_last_cuda_error",
                      "fa_device_error",
                      "fa_exp2_eval", "fa_exp2_sweep"):
@@ -131,6 +132,17 @@ def bwd_varlen(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, cu_seqlens, max
     _check("fa_bwd_varlen", lib().fa_bwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq_acc), _ptr(delta),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B, int(max_seqlen), T, H, D,
+        int(bool(causal)), float(scale), _stream(stream)))
+
+
+def bwd_varlen_deterministic(q, k, v, o, dout, lse, dq_acc, delta, dq_sem, dq, dk, dv, cu_seqlens,
+                             max_seqlen: int, causal: bool, scale: float, stream=None):
+    """fa_bwd_varlen_deterministic on caller-provided tensors (packed layout, fixed-order dQ)."""
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    _check("fa_bwd_varlen_deterministic", lib().fa_bwd_varlen_deterministic(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq_acc), _ptr(delta),
+        _ptr(dq_sem), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B, int(max_seqlen), T, H, D,
         int(bool(causal)), float(scale), _stream(stream)))
 
 
@@ -253,9 +265,10 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
 
 
 def backward_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: bool = False,
-                    scale: float | None = None, stream=None):
+                    scale: float | None = None, stream=None, deterministic: bool = False):
     """Exact attention backward over a packed batch (the forward_varlen
-    layout).  Returns (dq, dk, dv), bf16 [T, H, D]."""
+    layout).  Returns (dq, dk, dv), bf16 [T, H, D].  deterministic=True sums
+    dQ over key tiles in a fixed order (bitwise-repeatable results)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _check_packed(name, t, q.shape)
     _check_cu(cu_seqlens, q.device)
@@ -271,8 +284,15 @@ def backward_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: 
     dq_acc = ws[:acc_bytes].view(torch.float32)
     delta = ws[acc_bytes:acc_bytes + n * 4].view(torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    bwd_varlen(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, cu_seqlens, max_seqlen, causal,
-               scale, stream)
+    if deterministic:
+        B = cu_seqlens.numel() - 1
+        sem = torch.empty(bwd_semaphore_bytes(B, H, int(max_seqlen), D) // 4, dtype=torch.int32,
+                          device=q.device)
+        bwd_varlen_deterministic(q, k, v, o, dout, lse, dq_acc, delta, sem, dq, dk, dv, cu_seqlens,
+                                 max_seqlen, causal, scale, stream)
+    else:
+        bwd_varlen(q, k, v, o, dout, lse, dq_acc, delta, dq, dk, dv, cu_seqlens, max_seqlen,
+                   causal, scale, stream)
     return dq, dk, dv
 
 

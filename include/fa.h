@@ -197,6 +197,19 @@ fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, cons
                                int B, int H, int S, int D, int causal, float scale, void *stream);
 
 /*
+ * fa_bwd_deterministic over a packed batch (arguments as fa_bwd_varlen, plus
+ * dq_sem): every sequence's dQ is summed over its key tiles in a fixed order,
+ * so repeated calls give bitwise-identical dQ, dK and dV.
+ *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B, H, max_seqlen, D) bytes
+ *            (B = number of sequences), 16-byte aligned, contents ignored.
+ */
+fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                      const void *dout, const float *lse, float *dq_acc,
+                                      float *delta, int *dq_sem, void *dq, void *dk, void *dv,
+                                      const int *cu_seqlens, int B, int max_seqlen, int total,
+                                      int H, int D, int causal, float scale, void *stream);
+
+/*
  * Backward for callers that cannot allocate device memory: code that runs
  * where cudaMalloc is not allowed or not wanted (host callbacks, plug-ins
  * that only get their inputs and outputs from a host framework, tools that

@@ -32,6 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size",
+                 "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_deterministic", "fa_bwd_varlen_deterministic",
                  "fa_status_string",
                  "fa_last_cuda_error", "fa_device_error", "fa_exp2_eval", "fa_exp2_sweep"):
         assert must in names

@@ -157,3 +157,30 @@ def test_backward_d256_matches_fixed_length_kernel():
     torch.cuda.synchronize()
     assert torch.equal(dk.view(shp), dk2) and torch.equal(dv.view(shp), dv2)
     assert ((dq.view(shp).float() - dq2.float()).norm() / dq2.float().norm()).item() <= 1e-3
+
+
+@pytest.mark.parametrize("D,causal,H", [(128, False, 24), (128, True, 24), (64, True, 2),
+                                         (256, True, 2)])
+def test_backward_deterministic_packed(D, causal, H):
+    # fixed-order dQ over a packed batch: bit-for-bit repeatable, exact per
+    # sequence, and the atomic order's result up to the order of additions
+    # (H = 24 gives several rounds of the persistent grid)
+    lengths = [300, 1, 777, 128, 0, 513] if D != 256 else [300, 1, 200, 129]
+    q, k, v, do, cu = make_packed(lengths, H, D, seed=11)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd, dod, cud = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu.cuda()
+    mx = max(lengths)
+    o, lse = fa.forward_varlen(qd, kd, vd, cud, mx, causal=causal, scale=scale)
+    a = fa.backward_varlen(qd, kd, vd, o, dod, lse, cud, mx, causal=causal, scale=scale,
+                           deterministic=True)
+    b = fa.backward_varlen(qd, kd, vd, o, dod, lse, cud, mx, causal=causal, scale=scale,
+                           deterministic=True)
+    c = fa.backward_varlen(qd, kd, vd, o, dod, lse, cud, mx, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    for x, y in zip(a, c):
+        x, y = x.float(), y.float()
+        assert ((x - y).norm() / y.norm()).item() <= 2e-3
+    _check_bwd_each(q, k, v, do, cu, a[0].cpu(), a[1].cpu(), a[2].cpu(), causal, scale)

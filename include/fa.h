@@ -31,8 +31,9 @@
  *     means key j is visible to query i iff j <= i.
  *   - Errors: FA_ERR_INVALID_ARG for a null or misaligned pointer, a
  *     non-positive size, overflow or a bad scale; FA_ERR_UNSUPPORTED for a
- *     head dim outside the supported set or a device without tcgen05
- *     (compute capability 10.x); FA_ERR_CUDA when a CUDA call or launch
+ *     head dim outside the supported set or a device other than compute
+ *     capability 10.3 (the kernels are built for sm_103a only), and for
+ *     option combinations an entry point names; FA_ERR_CUDA when a CUDA call or launch
  *     fails (see fa_last_cuda_error).  Nothing is enqueued when an error is
  *     returned by the argument checks.
  *   - Device-side waits are bounded.  A wait that runs out (which correct

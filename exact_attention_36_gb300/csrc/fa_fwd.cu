@@ -293,11 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 if (!mbar_wait(q_full, qi & 1, w)) { ok = false; break; }
                 ++qi;
                 if constexpr (Cfg::kGrouped) {
-                    // Between two MMA groups the tensor pipe holds about one
-                    // queued MMA, so every wait or commit placed there idles it:
-                    // per key tile this issues [wait group, wait P0] PV0 S0
-                    // [commit, wait P1] PV1 S1 [commit].  Groups are released by
-                    // the softmax of tile 1 (S1(j+1) done: its last reader).
+                    // tcgen05.mma issue returns only when the pipe takes the
+                    // MMA, so the pipe has next to nothing queued when the
+                    // thread stops issuing: every wait or commit between two
+                    // MMA groups idles it for its whole length (measured: a
+                    // 64-cycle gap costs about 56).  Per key tile this issues
+                    // [wait group, wait P0] PV0 S0 [commit, wait P1] PV1 S1
+                    // [commit].  Groups are released by the softmax of tile 1
+                    // (S1(j+1), or S1(0) for {K_0}, done: the group's last reader).
                     uint32_t g = ring % Cfg::kGroups;
                     w.code = kErrFwdWait + 11;
                     if (!mbar_wait(&kv_full[g], (ring / Cfg::kGroups) & 1, w)) { ok = false; break; }

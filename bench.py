@@ -58,14 +58,15 @@ def load_peaks():
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # csv lines: timestamp, then the clock fields
+        self.regions = {}  # name -> (t0, t1), host wall-clock seconds
 
     def __enter__(self):
         try:
@@ -83,6 +84,41 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    @staticmethod
+    def _parse(line):
+        """(wall-clock seconds, [fields after the timestamp]) of one sample, or None."""
+        import datetime
+
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            return None
+        try:
+            t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+        return t, parts[1:]
+
+    def mark(self, name, t0, t1):
+        """Record the wall-clock span (time.time()) of a timed region, so that
+        its own samples can be told apart from the others'."""
+        self.regions[name] = (t0, t1)
+
+    def region_mhz(self, name):
+        """Median SM clock of the samples taken inside region `name` (None if none)."""
+        if name not in self.regions:
+            return None
+        t0, t1 = self.regions[name]
+        sm = []
+        for line in self.lines:
+            rec = self._parse(line)
+            if rec is None or not (t0 <= rec[0] <= t1):
+                continue
+            try:
+                sm.append(float(rec[1][0]))
+            except ValueError:
+                pass
+        return statistics.median(sm) if sm else None
+
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -93,12 +129,18 @@ class ClockSampler:
             self.thread.join(timeout=2)
 
     def summary(self):
+        """Median SM clock, max clock and throttle reasons over the samples
+        taken inside the marked timed regions (all samples if none marked)."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        spans = list(self.regions.values())
         for line in self.lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
+            rec = self._parse(line)
+            if rec is None:
                 continue
+            if spans and not any(t0 <= rec[0] <= t1 for t0, t1 in spans):
+                continue
+            parts = rec[1]
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
@@ -119,9 +161,12 @@ class ClockSampler:
 def oracle_sample(q, k, v, dout, causal, scale, rows):
     """Time the fp64 CPU oracle on a bounded sample of the workload: head
     (0, 0), the listed query rows: forward rows (O, LSE), the backward row
-    statistics (LSE, Delta) and the dQ rows.  Returns (seconds, metric FLOPs)
-    where the FLOPs are the metric's count for those rows: 4*S*D per row
-    forward and 2.5x that backward (halved under the causal mask)."""
+    statistics (LSE, Delta) and the dQ rows.  The dK/dV pass is not in the
+    sample (each key column needs every row's statistics, i.e. the whole
+    head).  Returns (seconds, FLOPs of the work that ran), counted the
+    metric's way per query row: 4*S*D forward, and of the backward's 10*S*D
+    the three products the dQ rows need (S recomputed, dP, dQ: 6*S*D);
+    halved under the causal mask."""
     import numpy as np
 
     import oracle
@@ -137,8 +182,12 @@ def oracle_sample(q, k, v, dout, causal, scale, rows):
     df[rows] = delta
     oracle.dq_rows_head(qh, kh, vh, dh, lf, df, causal, scale, rows)
     dt = time.perf_counter() - t0
-    per_row = 4.0 * S * D * (0.5 if causal else 1.0)
-    return dt, per_row * len(rows) * 3.5
+    per_row = (4.0 + 6.0) * S * D * (0.5 if causal else 1.0)
+    return dt, per_row * len(rows)
+
+
+SAMPLE_WHAT = ("forward, backward row statistics and dQ (not the dK/dV pass) for {n} of {S} "
+               "query rows of head (0,0)")
 
 
 def pick_rows(S, n, seed=0):
@@ -161,10 +210,11 @@ def cpu_sample(q, k, v, dout, causal, scale, target_s=12.0):
         n = int(min(S, max(2 * n, n * target_s / max(dt, 1e-3))))
         dt, fl = oracle_sample(q, k, v, dout, causal, scale, pick_rows(S, n, seed=2))
     return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": oracle.threads(), "kind": "oracle",
-            "sample": (f"fp64 CPU oracle, head (0,0) of {WORKLOAD['name']} "
-                       f"{'causal' if causal else 'non-causal'}: forward, backward row "
-                       f"statistics and dQ for {n} of {S} query rows ({dt:.1f} s); FLOPs "
-                       "counted as the metric counts them for those rows")}
+            "sample": (f"fp64 CPU oracle on {WORKLOAD['name']} "
+                       f"{'causal' if causal else 'non-causal'}: "
+                       + SAMPLE_WHAT.format(n=n, S=S)
+                       + f" ({dt:.1f} s); FLOPs: 4*S*D forward + 6*S*D (S, dP, dQ products) "
+                       "per sampled row, the metric's count for the work that ran")}
 
 
 # ---------------------------------------------------------------- GPU timing
@@ -187,6 +237,17 @@ class Buffers:
         self.delta = ws[acc_bytes:acc_bytes + n * 4].view(torch.float32)
         self.ws = ws
         self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.sem = None
+        if BWD_MODE.get("deterministic"):
+            self.sem = torch.empty(fa.bwd_semaphore_bytes(B, H, S, D) // 4, dtype=torch.int32,
+                                   device=dev)
+
+
+# forward numerics knobs of profiling runs (library defaults unless given)
+FWD_KNOBS = {}
+# backward variant of measurement runs: {"deterministic": True} times the
+# fixed-order dQ mode, {"pair_mode": 1} the CTA-pair kernel (defaults unless given)
+BWD_MODE = {}
 
 
 def run_step(buf, causal, scale, ev=None):
@@ -194,11 +255,15 @@ def run_step(buf, causal, scale, ev=None):
 
     if ev is not None:
         ev[0].record()
-    fa.fwd(buf.q, buf.k, buf.v, buf.o, buf.lse, causal, scale)
+    fa.fwd(buf.q, buf.k, buf.v, buf.o, buf.lse, causal, scale, **FWD_KNOBS)
     if ev is not None:
         ev[1].record()
-    fa.bwd(buf.q, buf.k, buf.v, buf.o, buf.dout, buf.lse, buf.dq_acc, buf.delta,
-           buf.dq, buf.dk, buf.dv, causal, scale)
+    if buf.sem is not None:
+        fa.bwd_deterministic(buf.q, buf.k, buf.v, buf.o, buf.dout, buf.lse, buf.dq_acc,
+                             buf.delta, buf.sem, buf.dq, buf.dk, buf.dv, causal, scale)
+    else:
+        fa.bwd(buf.q, buf.k, buf.v, buf.o, buf.dout, buf.lse, buf.dq_acc, buf.delta,
+               buf.dq, buf.dk, buf.dv, causal, scale, pair_mode=BWD_MODE.get("pair_mode", -1))
     if ev is not None:
         ev[2].record()
 
@@ -232,28 +297,32 @@ def job_tflops(world, flops_per_rank, ms_max):
 
 def time_device(buf, causal, scale, steps, warmup, dist_on):
     """Device-time K steps (CUDA events on the launching stream).  Returns
-    (ms per step, fwd ms per launch, bwd ms per call)."""
+    (ms per step, fwd ms per launch, bwd ms per call, (wall t0, wall t1) of
+    the timed region)."""
     for _ in range(warmup):
         run_step(buf, causal, scale)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist_on)
+    t0 = time.time()
     start.record()
     for i in range(steps):
         run_step(buf, causal, scale, evs[i])
     stop.record()
     barrier(dist_on)
+    t1 = time.time()
     total = start.elapsed_time(stop)
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
-    return max_over_ranks(total, dist_on) / steps, fwd_ms, bwd_ms
+    return max_over_ranks(total, dist_on) / steps, fwd_ms, bwd_ms, (t0, t1)
 
 
 def time_e2e(q, k, v, dout, buf, causal, scale, steps, warmup, dist_on):
     """The same step through the C ABI with host buffers.  Every step copies
     its Q, K, V, dO from pinned host memory and reads its dQ, dK, dV back;
     the copies run on a second stream, double-buffered, so step k+1's inputs
-    arrive while step k computes.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    arrive while step k computes.  Returns (ms per step, H2D bytes, D2H bytes,
+    (wall t0, wall t1) of the timed region)."""
     dev = buf.q.device
     hin = [t.pin_memory() for t in (q, k, v, dout)]
     hout = [[torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
@@ -294,44 +363,103 @@ def time_e2e(q, k, v, dout, buf, causal, scale, steps, warmup, dist_on):
 
     run(warmup)
     barrier(dist_on)
+    t0 = time.time()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(comp)
     run(steps)
     stop.record(comp)
     barrier(dist_on)
+    t1 = time.time()
     ms = max_over_ranks(start.elapsed_time(stop), dist_on) / steps
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = sum(t.numel() * t.element_size() for t in hout[0])
-    return ms, h2d, d2h
+    return ms, h2d, d2h, (t0, t1)
 
 
 # ---------------------------------------------------------------- main
 
 
-def kernel_source_hash():
-    """Hash of the CUDA sources: traffic figures recorded from an ncu capture
-    are only reported while the kernels they describe are unchanged."""
+# Translation units (and headers) that build each timed call; a traffic
+# figure recorded from an ncu capture is reported only while these files are
+# byte-for-byte what they were when it was captured.
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cu", "fa_api.cu", "fa_common.cuh", "sm100_ptx.cuh",
+                      "exp2_poly.cuh", "exp2_poly_coeffs.h"],
+    "fa_bwd": ["fa_bwd.cu", "fa_api.cu", "fa_common.cuh", "sm100_ptx.cuh"],
+}
+# ncu kernel names (prefix before the template arguments) of each call
+CALL_KERNELS = {
+    "fa_fwd_kernel": ["fa_fwd_kernel"],
+    "fa_bwd": ["fa_bwd_prep", "fa_bwd_kernel", "fa_bwd_dq_cvt"],
+}
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def source_hash(call):
+    """sha256 (first 16 hex digits) of the sources that build `call`."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_36_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[call]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+def recorded_traffic(call):
+    """DRAM bytes per call from the last ncu capture, or None when the
+    capture is missing or its kernels' sources have changed since."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
-    with open(path) as f:
+    with open(TRAFFIC_JSON) as f:
         rec = json.load(f)
-    ent = rec.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    ent = rec.get(call)
+    if not ent or ent.get("source_hash") != source_hash(call):
         return None
     return ent.get("bytes_per_launch")
+
+
+def record_traffic(csv_path, hashes_path, workload, command):
+    """Write profiles/traffic.json from an ncu --csv capture of
+    dram__bytes_read.sum / dram__bytes_write.sum over one bench step
+    (one launch of each kernel).  `hashes_path` holds the source hashes
+    printed by --source-hashes on the box in the same call as the capture;
+    a call whose sources differ here is refused."""
+    import csv
+
+    with open(hashes_path) as f:
+        box_hashes = json.load(f)
+    by_kernel = {}
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        name = row["Kernel Name"]
+        base = name.split("(")[0].split("<")[0].split("::")[-1].strip()
+        val = float(row["Metric Value"].replace(",", ""))
+        unit = row.get("Metric Unit", "byte").strip().lower()
+        mult = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
+        key = (row["ID"], base)
+        by_kernel.setdefault(key, 0.0)
+        by_kernel[key] += val * mult
+    per_base = {}
+    for (_, base), b in by_kernel.items():
+        per_base.setdefault(base, []).append(b)
+    out = {}
+    for call, kernels in CALL_KERNELS.items():
+        if box_hashes.get(call) != source_hash(call):
+            raise SystemExit(f"{call}: sources differ from the captured ones; not recorded")
+        if not all(k in per_base for k in kernels):
+            continue
+        per = {k: int(statistics.median(per_base[k])) for k in kernels}
+        out[call] = {"source_hash": source_hash(call), "sources": KERNEL_SOURCES[call],
+                     "bytes_per_launch": sum(per.values()), "per_kernel_bytes": per,
+                     "launches_seen": {k: len(per_base[k]) for k in kernels},
+                     "workload": workload, "command": command}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    return out
 
 
 def parse():
@@ -344,8 +472,27 @@ def parse():
                     help="skip the oracle timing (for quick runs)")
     ap.add_argument("--seq", type=int, default=WORKLOAD["S"],
                     help="sequence length override (profiling runs on a smaller case)")
+    ap.add_argument("--dim", type=int, default=WORKLOAD["D"],
+                    help="head dim override (profiling runs)")
+    ap.add_argument("--batch", type=int, default=WORKLOAD["B"],
+                    help="batch override (profiling runs)")
+    ap.add_argument("--poly-groups", type=int, default=-1,
+                    help="forward: columns of every 8 whose exp2 takes the FMA polynomial "
+                         "(profiling runs; -1 = library default)")
+    ap.add_argument("--poly-degree", type=int, default=-1,
+                    help="forward: degree of that polynomial, 3 or 5 (profiling runs)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the fixed-order (bitwise repeatable) backward (measurement runs)")
+    ap.add_argument("--pair", action="store_true",
+                    help="time the CTA-pair backward kernel, D = 128 (measurement runs)")
     ap.add_argument("--only-noncausal", action="store_true",
                     help="skip the causal measurement and the e2e loop (profiling runs)")
+    ap.add_argument("--source-hashes", action="store_true",
+                    help="print the source hash of each timed call and exit")
+    ap.add_argument("--record-traffic", nargs=2, metavar=("NCU_CSV", "HASHES_JSON"),
+                    help="write profiles/traffic.json from an ncu DRAM-bytes capture and exit")
+    ap.add_argument("--traffic-command", default="",
+                    help="with --record-traffic: the capture command, recorded beside it")
     return ap.parse_args()
 
 
@@ -373,8 +520,9 @@ def reference_arm(args, rank):
         times.append(dt)
     t = sum(times) / len(times)
     value = fl / t / 1e12
-    sample = (f"fp64 CPU oracle on head (0,0) of {W['name']} non-causal: forward, backward "
-              f"row statistics and dQ for {n} of {W['S']} query rows per step")
+    sample = (f"fp64 CPU oracle on {W['name']} non-causal, per step: "
+              + SAMPLE_WHAT.format(n=n, S=W["S"])
+              + "; FLOPs: 4*S*D forward + 6*S*D (S, dP, dQ products) per sampled row")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -390,6 +538,15 @@ def reference_arm(args, rank):
 
 def main():
     args = parse()
+    if args.source_hashes:
+        print(json.dumps({call: source_hash(call) for call in KERNEL_SOURCES}))
+        return
+    if args.record_traffic:
+        out = record_traffic(args.record_traffic[0], args.record_traffic[1],
+                             f"B{args.batch}_H16_S{args.seq}_D{args.dim} non-causal, one bench step",
+                             args.traffic_command)
+        print(json.dumps(out, indent=1))
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -410,9 +567,17 @@ def main():
 
     fa_build.build()
     W = dict(WORKLOAD)
-    if args.seq != W["S"]:
-        W["S"] = args.seq
-        W["name"] = f"B1_H16_S{args.seq}_D128"
+    W.update(B=args.batch, S=args.seq, D=args.dim)
+    W["name"] = f"B{W['B']}_H{W['H']}_S{W['S']}_D{W['D']}"
+    is_headline = (W["B"], W["S"], W["D"]) == (WORKLOAD["B"], WORKLOAD["S"], WORKLOAD["D"])
+    if args.poly_groups >= 0:
+        FWD_KNOBS["poly_exp2_groups"] = args.poly_groups
+    if args.poly_degree >= 0:
+        FWD_KNOBS["poly_exp2_degree"] = args.poly_degree
+    if args.deterministic:
+        BWD_MODE["deterministic"] = True
+    if args.pair:
+        BWD_MODE["pair_mode"] = 1
     B, H, S, D = W["B"], W["H"], W["S"], W["D"]
     scale = 1.0 / math.sqrt(D)
     # every rank draws its own batch (weak scaling over independent heads)
@@ -422,15 +587,19 @@ def main():
     peaks, peak_src = load_peaks()
 
     with ClockSampler(local_rank) as clk:
-        ms, fwd_ms, bwd_ms = time_device(buf, False, scale, args.steps, args.warmup, dist_on)
+        ms, fwd_ms, bwd_ms, span = time_device(buf, False, scale, args.steps, args.warmup,
+                                               dist_on)
+        clk.mark("noncausal", *span)
         if args.only_noncausal:
             ms_c = fwd_ms_c = bwd_ms_c = float("nan")
             e2e_ms, h2d, d2h = float("nan"), 0, 0
         else:
-            ms_c, fwd_ms_c, bwd_ms_c = time_device(buf, True, scale, args.steps, args.warmup,
-                                                   dist_on)
-            e2e_ms, h2d, d2h = time_e2e(q, k, v, do, buf, False, scale, args.steps,
-                                        args.warmup, dist_on)
+            ms_c, fwd_ms_c, bwd_ms_c, span = time_device(buf, True, scale, args.steps,
+                                                         args.warmup, dist_on)
+            clk.mark("causal", *span)
+            e2e_ms, h2d, d2h, span = time_e2e(q, k, v, do, buf, False, scale, args.steps,
+                                              args.warmup, dist_on)
+            clk.mark("e2e", *span)
     clocks = clk.summary()
     assert fa.device_error() == 0, "a bounded device wait ran out"
 
@@ -438,14 +607,31 @@ def main():
     ffc, fbc = flops(B, H, S, D, True)
     value = job_tflops(world, ff + fb, ms)
     fwd_tf, bwd_tf = ff / (fwd_ms * 1e-3) / 1e12, fb / (bwd_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    # The calls are timed one at a time inside a sub-second region, so the
+    # burst peak (a GEMM timed alone) is the denominator; the sustained one
+    # (a seconds-long GEMM loop, taken at a lower clock under the power cap)
+    # is reported beside it with the clock it was measured at.
+    peak = peaks["bf16_tflops"]
+    peak_sus = peaks.get("bf16_tflops_sustained")
     if bwd_ms >= fwd_ms:
-        dom, dom_ms, dom_fl = "fa_bwd (preprocess + main + dQ convert)", bwd_ms, fb
-        traffic = recorded_traffic("fa_bwd") if S == WORKLOAD["S"] else None
+        dom, dom_ms, dom_fl, call = "fa_bwd (preprocess + main + dQ convert)", bwd_ms, fb, "fa_bwd"
     else:
-        dom, dom_ms, dom_fl = "fa_fwd_kernel", fwd_ms, ff
-        traffic = recorded_traffic("fa_fwd_kernel") if S == WORKLOAD["S"] else None
+        dom, dom_ms, dom_fl, call = "fa_fwd_kernel", fwd_ms, ff, "fa_fwd_kernel"
+    traffic = recorded_traffic(call) if is_headline else None
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
+
+    def per_clock(fl, ms_call, mhz):
+        # clock-normalised: FLOP per SM cycle (of 8192 for the dense bf16
+        # tensor pipe) at the median SM clock sampled during the call's region
+        if mhz is None or not (ms_call == ms_call):
+            return None
+        cycles = ms_call * 1e-3 * mhz * 1e6
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        return {"sm_mhz": mhz, "kcycles": cycles / 1e3,
+                "flop_per_sm_cycle": fl / cycles / n_sm,
+                "frac_of_8192": fl / cycles / n_sm / 8192.0}
+
+    mhz_n, mhz_c = clk.region_mhz("noncausal"), clk.region_mhz("causal")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -453,23 +639,42 @@ def main():
         "data": "synthetic",
         "config": {"workload": W["name"], "B": B, "H": H, "S": S, "D": D, "causal": False,
                    "scale": scale, "inputs": "seeded N(0,1) bf16",
-                   "l2": "inputs larger than L2 (Q,K,V,dO = 512 MiB per step)",
+                   "l2": (f"inputs larger than L2 (Q,K,V,dO = {4 * B * S * H * D * 2 >> 20} MiB "
+                          "per step)"),
                    "parallelism": f"independent batch per GPU x{world}"},
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "fwd_pct_of_2250": 100 * fwd_tf / NOMINAL_PEAK_TFLOPS,
         "bwd_pct_of_2250": 100 * bwd_tf / NOMINAL_PEAK_TFLOPS,
         "pct_of_2250": 100 * value / world / NOMINAL_PEAK_TFLOPS,
+        "fwd_frac_of_burst": fwd_tf / peak, "bwd_frac_of_burst": bwd_tf / peak,
+        "clock_normalised": {"fwd": per_clock(ff, fwd_ms, mhz_n),
+                             "bwd": per_clock(fb, bwd_ms, mhz_n),
+                             "causal_fwd": per_clock(ffc, fwd_ms_c, mhz_c),
+                             "causal_bwd": per_clock(fbc, bwd_ms_c, mhz_c)},
         "causal": {"tflops": job_tflops(world, ffc + fbc, ms_c), "ms_per_step": ms_c,
                    "fwd_tflops": ffc / (fwd_ms_c * 1e-3) / 1e12,
-                   "bwd_tflops": fbc / (bwd_ms_c * 1e-3) / 1e12},
+                   "bwd_tflops": fbc / (bwd_ms_c * 1e-3) / 1e12,
+                   "fwd_frac_of_burst": ffc / (fwd_ms_c * 1e-3) / 1e12 / peak,
+                   "bwd_frac_of_burst": fbc / (bwd_ms_c * 1e-3) / 1e12 / peak},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained", "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic},
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_sustained": peak_sus,
+                     "peak_sustained_sm_mhz": peaks.get("clocks_under_load", {}).get(
+                         "sm_mhz_median"),
+                     "frac_of_sustained": achieved / peak_sus if peak_sus else None,
+                     "sm_mhz_during_call": mhz_n},
         "e2e": {"value": job_tflops(world, ff + fb, e2e_ms), "unit": "TFLOPS",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,  # fa_fwd 1 + fa_bwd 3 per step of the value's region
+        # fa_fwd 1 + fa_bwd 3 (4 in the fixed-order mode) per step of the value's region
+        "gpu_launches": (5 if args.deterministic else 4) * args.steps,
         "clocks": clocks,
     }
+    if FWD_KNOBS:
+        line["config"]["forward_knobs"] = dict(FWD_KNOBS)
+    if BWD_MODE:
+        line["config"]["backward_mode"] = dict(BWD_MODE)
     if args.only_noncausal:
         line["causal"] = None
         line["e2e"] = None

@@ -13,10 +13,23 @@ Tolerances (stated by the task for this method, not by the pages):
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
 import oracle
+
+# When set, the checks append one JSON line per checked case to this file
+# (the per-case errors behind the gates, for a written test report).
+REPORT = os.environ.get("FA_PARITY_REPORT")
+
+
+def _record(entry):
+    if REPORT:
+        with open(REPORT, "a") as f:
+            f.write(json.dumps(entry) + "\n")
 
 O_ATOL = 1e-2
 LSE_ATOL = 1e-3
@@ -29,17 +42,21 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.where(ax > 0, 2.0 ** (e - 8), 0.0)
 
 
-def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None, peaked=False):
+def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None, peaked=False, case=None):
     """Compare GPU o [B,S,H,D] / lse [B,H,S] with the oracle on the listed
     heads (and rows).  Returns (max O error, max LSE error).
 
     peaked=True (the stress inputs: scores ~30x the N(0,1) scale, nearly
     one-hot rows): P enters the PV product rounded to bf16 (relative 2^-9,
-    FlashAttention-4 pages: bf16 quantisation dominates), which alone can move
-    O by up to 2^-9 max|V|; with the output's own half-ulp that can exceed the
-    plain gate.  The bound asserted is then 1e-2 + ulp/2 + 2^-8 max|V| (the
-    P-rounding bound with a factor 2 for the fp32 products around it), and at
-    most 1e-5 of the elements may exceed the plain gate."""
+    FlashAttention-4 pages: bf16 quantisation dominates).  With p_j the fp32
+    probabilities, l their sum and P_j = p_j (1 + e_j), |e_j| <= 2^-9, the
+    product moves O by |sum_j p_j e_j V_j| / l <= 2^-9 max|V| (the fp32 sums
+    add relative errors of order 2^-24, far below that).  With the output's
+    own half-ulp that can exceed the plain gate, so the bound asserted is
+    1e-2 + ulp/2 + 2^-9 max|V|, and at most 1e-5 of the elements may exceed
+    the plain gate.
+
+    case: a label; with FA_PARITY_REPORT set, the errors are recorded."""
     ref = oracle.forward(q, k, v, causal, scale, heads=heads, rows=rows)
     o_cpu = o.float().cpu()
     lse_cpu = lse.cpu()
@@ -54,12 +71,17 @@ def check_forward(q, k, v, o, lse, causal, scale, heads, rows=None, peaked=False
             lg = lse_cpu[b, h, idx].double().numpy()
         err = np.abs(og - o_ref)
         tol = O_ATOL + half_ulp_bf16(o_ref)
+        over = int((err > tol).sum())
+        vmax = float(np.abs(_f64_head(v, b, h)).max())
+        if case is not None:
+            _record({"dir": "fwd", "case": case, "head": [b, h], "o_max_err": float(err.max()),
+                     "o_ref_max_abs": float(np.abs(o_ref).max()), "v_max_abs": vmax,
+                     "over_plain_gate": over, "elements": int(err.size),
+                     "lse_max_err": float(np.abs(lg - lse_ref).max()), "peaked": peaked})
         if peaked:
-            vmax = float(np.abs(_f64_head(v, b, h)).max())
-            over = int((err > tol).sum())
             assert over <= max(1, int(1e-5 * err.size)), (
                 f"{over} of {err.size} O elements above the plain gate in head {(b, h)}")
-            tol = tol + 2.0 ** -8 * vmax
+            tol = tol + 2.0 ** -9 * vmax
         bad = err > tol
         assert not bad.any(), (
             f"O mismatch head {(b, h)}: max err {err.max():.4g}, "
@@ -80,7 +102,8 @@ def rel_l2(got: np.ndarray, want: np.ndarray) -> float:
     return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), floor))
 
 
-def check_backward(q, k, v, dout, dq, dk, dv, causal, scale, heads, rows=None, cols=None):
+def check_backward(q, k, v, dout, dq, dk, dv, causal, scale, heads, rows=None, cols=None,
+                   case=None):
     """Compare GPU gradients with the oracle's (exact fp64) gradients on the
     listed heads (rows of dQ / key columns of dK, dV).  Returns the worst
     relative L2 error per tensor."""
@@ -96,9 +119,11 @@ def check_backward(q, k, v, dout, dq, dk, dv, causal, scale, heads, rows=None, c
             acc[name][1].append(g[name])
     worst = {}
     for name, (gs, ws) in acc.items():
-        e = rel_l2(np.concatenate(gs), np.concatenate(ws))
+        worst[name] = rel_l2(np.concatenate(gs), np.concatenate(ws))
+    if case is not None:
+        _record({"dir": "bwd", "case": case, **{f"{n}_rel_l2": e for n, e in worst.items()}})
+    for name, e in worst.items():
         assert e <= GRAD_REL_L2, f"{name} relative L2 error {e:.4g} > {GRAD_REL_L2}"
-        worst[name] = e
     return worst
 
 

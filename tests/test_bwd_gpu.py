@@ -73,7 +73,8 @@ def test_stress_sweep(S, B, D, causal):
     q, k, v, do, dq, dk, dv, scale = _run(B, 16, S, D, causal, stress=True)
     rows = None if S <= 4096 else sample_rows(S, 128, seed=5)
     check_backward(q, k, v, do, dq, dk, dv, causal, scale, heads=[(0, 0), (B - 1, 15)],
-                   rows=rows, cols=rows)
+                   rows=rows, cols=rows,
+                   case=f"B{B}_H16_S{S}_D{D}_{'causal' if causal else 'noncausal'}")
 
 
 def _invariants(do, dk, dv):

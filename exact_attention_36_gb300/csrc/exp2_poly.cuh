@@ -64,20 +64,34 @@ __device__ __forceinline__ float exp2_poly_full(float x) {
 }
 
 // Two lanes at once, the kernel variant's arithmetic with two-lane fp32
-// instructions (same rounding, same results as exp2_poly<3> per lane).
-__device__ __forceinline__ float2 exp2_poly3_x2(float2 x) {
+// instructions (same rounding, same results as exp2_poly<DEG> per lane).
+template <int DEG>
+__device__ __forceinline__ float2 exp2_poly_x2(float2 x) {
     const float2 kShift = make_float2(12582912.0f, 12582912.0f);
     x.x = fmaxf(x.x, -125.0f);
     x.y = fmaxf(x.y, -125.0f);
     const float2 t = add2(x, kShift);
     const float2 n = add2(t, make_float2(-12582912.0f, -12582912.0f));
     const float2 f = fma2(n, make_float2(-1.0f, -1.0f), x);
-    float2 p = fma2(make_float2(FA_EXP2_P3_C3, FA_EXP2_P3_C3), f,
-                    make_float2(FA_EXP2_P3_C2, FA_EXP2_P3_C2));
-    p = fma2(p, f, make_float2(FA_EXP2_P3_C1, FA_EXP2_P3_C1));
-    p = fma2(p, f, make_float2(FA_EXP2_P3_C0, FA_EXP2_P3_C0));
+    float2 p;
+    if constexpr (DEG == 5) {
+        p = fma2(make_float2(FA_EXP2_P5_C5, FA_EXP2_P5_C5), f,
+                 make_float2(FA_EXP2_P5_C4, FA_EXP2_P5_C4));
+        p = fma2(p, f, make_float2(FA_EXP2_P5_C3, FA_EXP2_P5_C3));
+        p = fma2(p, f, make_float2(FA_EXP2_P5_C2, FA_EXP2_P5_C2));
+        p = fma2(p, f, make_float2(FA_EXP2_P5_C1, FA_EXP2_P5_C1));
+        p = fma2(p, f, make_float2(FA_EXP2_P5_C0, FA_EXP2_P5_C0));
+    } else {
+        static_assert(DEG == 3, "degree 3 or 5");
+        p = fma2(make_float2(FA_EXP2_P3_C3, FA_EXP2_P3_C3), f,
+                 make_float2(FA_EXP2_P3_C2, FA_EXP2_P3_C2));
+        p = fma2(p, f, make_float2(FA_EXP2_P3_C1, FA_EXP2_P3_C1));
+        p = fma2(p, f, make_float2(FA_EXP2_P3_C0, FA_EXP2_P3_C0));
+    }
     return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
                        __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
 }
+
+__device__ __forceinline__ float2 exp2_poly3_x2(float2 x) { return exp2_poly_x2<3>(x); }
 
 }  // namespace fa

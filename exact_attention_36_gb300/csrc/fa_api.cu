@@ -139,11 +139,21 @@ fa_status check_shape(int B, int H, int S, int D, float scale) {
     return FA_OK;
 }
 
-// Deterministic-mode scratch: counters [B*H][ceil(S/64)], then the order keys
-// [B*H][ceil(S/128)] of the key tiles; each part padded to 256 bytes.
-size_t sem_counter_bytes(int B, int H, int S) {
-    const size_t n = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 63) / 64);
-    return (n * sizeof(int) + 255) & ~static_cast<size_t>(255);
+size_t pad256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Deterministic-mode scratch at D = 64 and 128: turn counters
+// [B*H][ceil(S/128)][4 drain warps][2 accumulators], the order keys
+// [B*H][ceil(S/128)] of the key tiles, then the second fp32 dQ accumulator
+// over all query rows; each part padded to 256 bytes.  At D = 256: counters
+// [B*H][2 halves][ceil(S/64)][4 drain warps] only.
+size_t det_counter_bytes(int B, int H, int S) {
+    return pad256(static_cast<size_t>(B) * H * 8 * ((static_cast<size_t>(S) + 127) / 128) * 4);
+}
+size_t det_key_bytes(int B, int H, int S) {
+    return pad256(static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 127) / 128) * 4);
+}
+size_t d256_counter_bytes(int B, int H, int S) {
+    return pad256(static_cast<size_t>(B) * H * 8 * ((static_cast<size_t>(S) + 63) / 64) * 4);
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -152,6 +162,7 @@ constexpr float kDefaultRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 betwee
 // polynomial gives 1419 TFLOPS, 1 gives 1380, 2 gives 1318, 8 gives 970; its
 // MUFU keeps up with the tensor core, so the default leaves exp2 on MUFU.
 constexpr int kDefaultPolyGroups = 0;
+constexpr int kDefaultPolyDegree = 3;  // the cheaper of the two degrees the method allows
 
 }  // namespace
 
@@ -164,6 +175,7 @@ __device__ __forceinline__ float exp2_variant(float x, int variant) {
     if (variant == 1) return fa::exp2_poly_full<3>(x);
     if (variant == 3) return fa::exp2_poly3_x2(make_float2(x, -x)).x;
     if (variant == 4) return fa::exp2_poly_full<5>(x);
+    if (variant == 5) return fa::exp2_poly_x2<5>(make_float2(x, -x)).x;
     return fa::ex2_mufu(x);
 }
 
@@ -264,7 +276,8 @@ namespace {
 // else packed: B sequences in [T, H, D], S = the longest.
 fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu,
                    int B, int H, int S, int T, int D, int causal, float scale,
-                   float rescale_threshold, int poly_exp2_groups, void *stream) {
+                   float rescale_threshold, int poly_exp2_groups, int poly_exp2_degree,
+                   void *stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
@@ -278,6 +291,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     if (poly_exp2_groups != 0 && poly_exp2_groups != 1 && poly_exp2_groups != 2 &&
         poly_exp2_groups != 8)
         return FA_ERR_INVALID_ARG;
+    if (poly_exp2_degree < 0) poly_exp2_degree = kDefaultPolyDegree;
+    if (poly_exp2_degree != 3 && poly_exp2_degree != 5) return FA_ERR_INVALID_ARG;
     const DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != FA_OK) return st;
     if ((st = get_encoder()) != FA_OK) return st;
@@ -297,6 +312,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     a.scale_log2 = scale * kLog2e;
     a.rescale_threshold = rescale_threshold;
     a.poly_groups = poly_exp2_groups;
+    a.poly_degree = poly_exp2_degree;
     a.err_word = d->err_word;
     a.num_sms = d->num_sms;
     a.cu_seqlens = cu;
@@ -311,9 +327,9 @@ extern "C" {
 
 fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                     int H, int S, int D, int causal, float scale, float rescale_threshold,
-                    int poly_exp2_groups, void *stream) {
+                    int poly_exp2_groups, int poly_exp2_degree, void *stream) {
     return fwd_impl(q, k, v, o, lse, nullptr, B, H, S, 0, D, causal, scale, rescale_threshold,
-                    poly_exp2_groups, stream);
+                    poly_exp2_groups, poly_exp2_degree, stream);
 }
 
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -321,12 +337,12 @@ fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, fl
                         int causal, float scale, void *stream) {
     if (!cu_seqlens) return FA_ERR_INVALID_ARG;
     return fwd_impl(q, k, v, o, lse, cu_seqlens, B, H, max_seqlen, total, D, causal, scale, -1.f,
-                    -1, stream);
+                    -1, -1, stream);
 }
 
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                  int S, int D, int causal, float scale, void *stream) {
-    return fa_fwd_ex(q, k, v, o, lse, B, H, S, D, causal, scale, -1.f, -1, stream);
+    return fa_fwd_ex(q, k, v, o, lse, B, H, S, D, causal, scale, -1.f, -1, -1, stream);
 }
 
 static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -389,9 +405,15 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     a.dq_acc = dq_acc;
     a.delta = delta;
     a.dq_sem = sem;
-    a.dq_key = (sem && D != 256)
-                   ? reinterpret_cast<int *>(reinterpret_cast<char *>(sem) + sem_counter_bytes(B, H, S))
-                   : nullptr;
+    if (sem && D != 256) {
+        // fixed order at D = 64/128: order keys, then the second accumulator
+        char *base = reinterpret_cast<char *>(sem);
+        a.dq_key = reinterpret_cast<int *>(base + det_counter_bytes(B, H, S));
+        a.dq_acc2 = reinterpret_cast<float *>(base + det_counter_bytes(B, H, S) +
+                                              det_key_bytes(B, H, S));
+        if ((st = make_map_dqacc(&a.tm_dqacc2, a.dq_acc2, mb * H, ms, D, dqrows)) != FA_OK)
+            return st;
+    }
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -455,9 +477,17 @@ fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *
 
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D) {
     if (check_shape(B, H, S, D, 1.f) != FA_OK) return 0;
-    if (D == 256) return 2 * sem_counter_bytes(B, H, S);  // one counter set per output half
-    const size_t u = static_cast<size_t>(B) * H * ((static_cast<size_t>(S) + 127) / 128);
-    return sem_counter_bytes(B, H, S) + ((u * sizeof(int) + 255) & ~static_cast<size_t>(255));
+    if (D == 256) return d256_counter_bytes(B, H, S);  // one counter set per output half
+    return det_counter_bytes(B, H, S) + det_key_bytes(B, H, S) +
+           pad256(static_cast<size_t>(B) * H * S * D * 4);
+}
+
+size_t fa_bwd_varlen_semaphore_bytes(int B, int max_seqlen, int total, int H, int D) {
+    if (B < 1 || max_seqlen < 1 || max_seqlen > total) return 0;
+    if (check_shape(1, H, total, D, 1.f) != FA_OK) return 0;
+    if (D == 256) return d256_counter_bytes(B, H, max_seqlen);
+    return det_counter_bytes(B, H, max_seqlen) + det_key_bytes(B, H, max_seqlen) +
+           pad256(static_cast<size_t>(H) * total * D * 4);
 }
 
 fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
@@ -470,7 +500,7 @@ fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, cons
 }
 
 fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void *stream) {
-    if (!x || !y || n < 0 || variant < 0 || variant > 4) return FA_ERR_INVALID_ARG;
+    if (!x || !y || n < 0 || variant < 0 || variant > 5) return FA_ERR_INVALID_ARG;
     if (n == 0) return FA_OK;
     const DeviceInfo *d = nullptr;
     fa_status st = device_info(&d);
@@ -484,7 +514,7 @@ fa_status fa_exp2_eval(const float *x, float *y, long long n, int variant, void 
 
 fa_status fa_exp2_sweep(float lo, float hi, int variant, double *out, void *stream) {
     if (!out || !(std::isfinite(lo) && std::isfinite(hi)) || lo > hi || variant < 0 ||
-        variant > 4)
+        variant > 5)
         return FA_ERR_INVALID_ARG;
     const DeviceInfo *d = nullptr;
     fa_status st = device_info(&d);

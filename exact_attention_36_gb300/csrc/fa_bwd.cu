@@ -81,7 +81,7 @@ struct BwdCfg {
     static constexpr int kOffBar = kOffDb + kBias;
     // kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full,
     // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dkdv_empty, drain
-    static constexpr int kNumBars = 18;
+    static constexpr int kNumBars = 17;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     // no alignment slack: the dynamic shared memory base must be 1024-byte
     // aligned (checked at kernel entry)
@@ -315,7 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     uint64_t *dq_full = bars + 12, *dq_empty = bars + 13;
     uint64_t *dkdv_full = bars + 14, *dkdv_empty = bars + 15;
     uint64_t *drain = bars + 16;
-    uint64_t *rel_bar = bars + 17;  // fixed-order mode: the four drain warps' reductions done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
@@ -325,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     const int BH = args.B * H;
     const int nT = (S + kBlk - 1) / kBlk;  // key tiles = query blocks
     const int U = BH * nT;
-    const int nSem = (S + 63) / 64;        // deterministic-mode counters per head
+    const int nSem = 8 * nT;               // deterministic-mode counters per head
     const bool rotate = kDet && !args.causal;  // see block_at
 
     if (threadIdx.x == 0) {
@@ -346,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         mbar_init(dkdv_full, 1);
         mbar_init(dkdv_empty, 128);
         mbar_init(drain, 1);
-        mbar_init(rel_bar, 4);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -690,17 +688,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // TMEM lane: query (dQ) or key (dK, dV)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const bool leader = (threadIdx.x == 256);
         uint8_t *stage = smem + Cfg::kOffRed + quarter * 4096;
         uint8_t *stage_row = stage + lane * 128;
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 40};
-        // fixed-order mode: one block's contribution is complete in L2 in all
-        // four warps (each arrives on rel_bar and waits, bounded, for the
-        // other three, so no warp runs a block ahead), then the leader
-        // advances the block's counter
         // each warp stages its 32 query rows of dQ_i, 32 columns at a time, and
         // reduces them on its own (no wait on the other drain warps)
-        auto stage_and_reduce = [&](const uint32_t (&acc)[D], int row0, int z, bool go) {
+        auto stage_and_reduce = [&](const uint32_t (&acc)[D], int row0, int z, bool go,
+                                    const CUtensorMap *map) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 if (lane == 0) bulk_wait_read<0>();  // the previous reduction has read buf
@@ -713,23 +707,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && go && !*abort_flag) {
-                    tma_reduce_add_3d(&args.tm_dqacc, stage, 32 * c, row0, z);
+                    tma_reduce_add_3d(map, stage, 32 * c, row0, z);
                     bulk_commit();
                 }
             }
         };
+        // Fixed-order mode: each drain warp has its own turn counters (its 32
+        // query rows of a block), so the four warps never wait on one another
+        // here.  A turn is passed on once this warp's reductions of the block
+        // are complete: wait for its bulk groups, order their (async-proxy)
+        // writes before the release, then a release add on the counter.
         int *sem_prev = nullptr;
-        uint32_t nrel = 0;
         auto release_block = [&](int *sem_done) {
             if (lane == 0) {
                 bulk_wait<0>();
                 fence_proxy_async_global();
-                __threadfence();
-                mbar_arrive(rel_bar);
-                w.code = kErrBwdWait + 43;
-                if (mbar_wait(rel_bar, nrel & 1, w) && leader) red_release_gpu_add(sem_done, 1);
+                red_release_gpu_add(sem_done, 1);
             }
-            ++nrel;
         };
         uint32_t n = 0, nunit = 0;
         bool ok = true;
@@ -761,32 +755,42 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 tc_fence_before();
                 mbar_arrive(dq_empty);
                 if constexpr (kDet) {
-                    // Fixed order: key tile j adds its share of dQ block i when
-                    // the block's counter reaches its place in the sum
-                    // (dq_position).  The previous block's counter is released
-                    // first, a block period after its reductions were issued (so
-                    // they are complete) and independently of this block's wait:
-                    // releases follow only this CTA's own progress, which keeps
-                    // the waits between tiles acyclic.
+                    // Fixed order: key tile j's share of dQ block i has a place
+                    // p in the block's sum (dq_position / causal_rank).  Places
+                    // alternate between two accumulators: p goes into
+                    // accumulator p % 2 as its (p / 2)-th term, so consecutive
+                    // contributions do not wait on each other, and each
+                    // accumulator's order is still fixed (the convert kernel
+                    // adds the two in a fixed order).  This warp waits until
+                    // the counter of (block, its 32 rows, accumulator) reaches
+                    // p / 2.  Its counter of the previous block is released
+                    // first, a block period after its reductions were issued
+                    // (so they are complete) and independently of this block's
+                    // wait: a release needs only this CTA's own progress (its
+                    // warps' earlier turns), which keeps the waits between
+                    // tiles acyclic.
                     if (sem_prev) {
                         release_block(sem_prev);
                         sem_prev = nullptr;
                     }
-                    int *sem = args.dq_sem + static_cast<size_t>(un.bh) * nSem + (i * kBlk) / 64;
                     const int place =
                         args.causal ? causal_rank(args.dq_key + static_cast<size_t>(un.bh) * nT, un.j, i, lane)
                                     : dq_position(un.bh, un.j, i, nT, nb, gridDim.x);
+                    int *sem = args.dq_sem + static_cast<size_t>(un.bh) * nSem + 8 * i + 2 * quarter +
+                               (place & 1);
                     bool go = true;
                     if (lane == 0) {
                         w.code = kErrBwdWait + 42;
-                        go = counter_wait_geq(sem, place, w);
+                        go = counter_wait_geq(sem, place >> 1, w);
                         fence_proxy_async_global();
                     }
                     go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, go);
+                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, go,
+                                     (place & 1) ? &args.tm_dqacc2 : &args.tm_dqacc);
                     sem_prev = sem;
                 } else {
-                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, true);
+                    stage_and_reduce(acc, acc_row0 + i * kBlk + quarter * 32, acc_z, true,
+                                     &args.tm_dqacc);
                 }
             }
             if (kDet && sem_prev) {  // the unit's last block
@@ -870,6 +874,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdAr
     float4 *z = reinterpret_cast<float4 *>(args.dq_acc + static_cast<size_t>(row) * D);
 #pragma unroll
     for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (args.dq_acc2) {  // fixed-order mode: the second accumulator too
+        float4 *z2 = reinterpret_cast<float4 *>(args.dq_acc2 + static_cast<size_t>(row) * D);
+#pragma unroll
+        for (int e = lane; e < D / 4; e += 32) z2[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
 // Fixed-order mode: zero the counters (one per (sequence, head, 64 rows) of
@@ -879,7 +888,10 @@ __global__ void __launch_bounds__(256) fa_bwd_prep(const __grid_constant__ BwdAr
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_det_setup(const __grid_constant__ BwdArgs args) {
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long nctr = static_cast<long long>(args.B) * args.H * ((args.S + 63) / 64) * (D == 256 ? 2 : 1);
+    // D = 64/128: eight per 128-query block (drain warp x accumulator); D =
+    // 256: four per 64-query block and output half (one per drain warp)
+    const long long nctr = static_cast<long long>(args.B) * args.H *
+                           (D == 256 ? 8 * ((args.S + 63) / 64) : 8 * ((args.S + kBlk - 1) / kBlk));
     if (t < nctr) args.dq_sem[t] = 0;
     if constexpr (D != 256) {
         if (args.dq_key && args.causal) {
@@ -895,7 +907,8 @@ __global__ void __launch_bounds__(256) fa_bwd_det_setup(const __grid_constant__ 
     }
 }
 
-// One warp per (b, h, query row): dQ[b, q, h, :] = bf16(scale * accumulator).
+// One warp per (b, h, query row): dQ[b, q, h, :] = bf16(scale * accumulator)
+// (fixed-order mode: bf16(scale * (accumulator + second accumulator))).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_cvt(const __grid_constant__ BwdArgs args) {
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -909,6 +922,16 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_cvt(const __grid_constant__ Bwd
     const float *src = args.dq_acc + static_cast<size_t>(row) * D;
     uint32_t *dst = reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(args.dq) +
                                                  ((static_cast<size_t>(b) * S + q) * H + h) * D);
+    if (args.dq_acc2) {
+        const float *src2 = args.dq_acc2 + static_cast<size_t>(row) * D;
+#pragma unroll
+        for (int e = lane; e < D / 2; e += 32) {
+            const float2 a = reinterpret_cast<const float2 *>(src)[e];
+            const float2 a2 = reinterpret_cast<const float2 *>(src2)[e];
+            dst[e] = pack_bf16x2((a.x + a2.x) * args.scale, (a.y + a2.y) * args.scale);
+        }
+        return;
+    }
 #pragma unroll
     for (int e = lane; e < D / 2; e += 32) {
         const float2 a = reinterpret_cast<const float2 *>(src)[e];
@@ -920,7 +943,8 @@ template <int D>
 cudaError_t launch_det_setup(const BwdArgs &a, int grid, cudaStream_t stream) {
     BwdArgs sa = a;
     sa.grid = grid;
-    const long long nctr = static_cast<long long>(a.B) * a.H * ((a.S + 63) / 64) * (D == 256 ? 2 : 1);
+    const long long nctr = static_cast<long long>(a.B) * a.H *
+                           (D == 256 ? 8 * ((a.S + 63) / 64) : 8 * ((a.S + kBlk - 1) / kBlk));
     const long long U = static_cast<long long>(a.B) * a.H * ((a.S + kBlk - 1) / kBlk);
     const long long n = nctr > U ? nctr : U;
     fa_bwd_det_setup<D><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(sa);

@@ -40,7 +40,7 @@ struct Cfg {
     static constexpr int kOffRed = kOffDS + 16384;    // 2 x (64 rows x 32 fp32) dQ staging
     static constexpr int kOffStat = kOffRed + 16384;  // 64 lse2 + 64 delta
     static constexpr int kOffBar = kOffStat + 512;
-    static constexpr int kNumBars = 16;
+    static constexpr int kNumBars = 15;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked)
     static constexpr uint32_t kTX = 0, kTY = 64, kTdV = 128, kTdK = 256;
@@ -90,7 +90,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
     uint64_t *dq_full = bars + 10, *dq_empty = bars + 11;
     uint64_t *dkdv_full = bars + 12, *dkdv_empty = bars + 13;
     uint64_t *drain = bars + 14;
-    uint64_t *rel_bar = bars + 15;  // fixed-order mode: the four drain warps' reductions done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
     float *stat = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // lse2[64] | delta[64]
@@ -118,7 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
         mbar_init(dkdv_full, 1);
         mbar_init(dkdv_empty, 128);
         mbar_init(drain, 1);
-        mbar_init(rel_bar, 4);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -405,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         uint8_t *stage = smem + Cfg::kOffRed + quarter * 4096;
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x80};
-        uint32_t n = 0, nunit = 0, nrel = 0;
+        uint32_t n = 0, nunit = 0;
         const int nQs = (S + kQB - 1) / kQB;  // fixed-order counters per head and half
         bool ok = true;
         for (int it = 0; ok; ++it) {
@@ -431,14 +429,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                 tc_fence_before();
                 mbar_arrive(dq_empty);
                 // Fixed-order mode: the key tiles add their shares of this
-                // (head, half, 64-query block) in ascending order.  Units are
+                // (head, half, 64-query block) in ascending order, each drain
+                // warp (32 columns of the half) under its own counter.  Units are
                 // numbered with ascending key tiles within a head and half and
                 // taken in rounds by the persistent grid, so a tile waits only
                 // for units of its own round or of earlier ones (no cycle).
                 int *sem = nullptr;
                 bool go = true;
                 if constexpr (kDet) {
-                    sem = args.dq_sem + (static_cast<size_t>(un.bh) * 2 + un.oh) * nQs + i;
+                    // this warp's counter: its 32 columns of the (head, half,
+                    // 64-query block)
+                    sem = args.dq_sem + ((static_cast<size_t>(un.bh) * 2 + un.oh) * nQs + i) * 4 +
+                          quarter;
                     if (lane == 0) {
                         w.code = kErrBwdWait + 0x82;
                         go = counter_wait_geq(sem, un.j, w);
@@ -463,17 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     }
                 }
                 if (kDet && sem) {
-                    // this block's share is complete in L2 in all four warps,
-                    // then the first of them passes the turn on
+                    // this warp's share of the block is complete in L2: its
+                    // (async-proxy) reductions are ordered before the release
+                    // that passes the turn on
                     if (lane == 0) {
                         bulk_wait<0>();
                         fence_proxy_async_global();
-                        __threadfence();
-                        mbar_arrive(rel_bar);
-                        w.code = kErrBwdWait + 0x83;
-                        if (mbar_wait(rel_bar, nrel & 1, w) && quarter == 0) red_release_gpu_add(sem, 1);
+                        red_release_gpu_add(sem, 1);
                     }
-                    ++nrel;
                 }
             }
             if (!ok) break;

@@ -26,6 +26,7 @@ struct FwdArgs {
     float scale_log2;         // softmax scale * log2(e)
     float rescale_threshold;  // log2 units
     int poly_groups;          // columns of every 8 whose exp2 uses the FMA polynomial
+    int poly_degree;          // that polynomial's degree: 3 or 5
     int *err_word;            // device error word
     int num_sms;
     const int *cu_seqlens;    // packed variable-length batch: B+1 offsets, else null
@@ -40,8 +41,14 @@ struct BwdArgs {
     const float *lse;                     // fp32 [B,H,S]
     float *dq_acc;                        // fp32 [B,H,S,D]
     float *delta;                         // fp32 [B,H,S]
-    int *dq_sem;                          // deterministic mode: [B*H][ceil(S/64)] counters, else null
+    int *dq_sem;                          // deterministic mode: turn counters, else null
+                                          // (D = 64/128: [B*H][ceil(S/128)][4 drain warps]
+                                          // [2 accumulators]; D = 256: [B*H][2 halves]
+                                          // [ceil(S/64)][4 drain warps])
     int *dq_key;                          // deterministic mode: [B*H][ceil(S/128)] order keys of the key tiles
+    CUtensorMap tm_dqacc2;                // deterministic mode, D = 64/128: the second accumulator
+    float *dq_acc2;                       // deterministic mode, D = 64/128: second fp32 dQ
+                                          // accumulator (the layout of dq_acc), else null
     int grid;                             // main kernel's persistent grid (for the order keys)
     void *dq, *dk, *dv;                   // bf16 [B,S,H,D]
     int B, H, S, D;

@@ -127,7 +127,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_sa
                (acc || kk > 0) ? 1u : 0u);
 }
 
-template <int D, int POLY_PER8>
+// POLY_PER8: columns of every 8 whose exp2 takes the FMA polynomial;
+// POLY_DEG: that polynomial's degree (3 or 5)
+template <int D, int POLY_PER8, int POLY_DEG>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs args) {
     using Cfg = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -504,8 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     m_used = m_new;
                 }
                 // p = 2^(s*c2 - m_used): in every group of 8 columns the last
-                // POLY_PER8 go to the FMA polynomial, the rest to MUFU, so both
-                // units work at once; arguments and row sums use two-lane fp32
+                // POLY_PER8 go to the FMA polynomial (degree POLY_DEG), the rest
+                // to MUFU, so both units work at once; arguments and row sums
+                // use two-lane fp32
                 const float2 c2v = make_float2(c2, c2);
                 const float2 nmv = make_float2(-m_used, -m_used);
                 float2 lsum[4];
@@ -518,9 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         const float2 xv = fma2(make_float2(__uint_as_float(sr[c][e]),
                                                            __uint_as_float(sr[c][e + 1])),
                                                c2v, nmv);
+                        // columns e, e+1 of their group of 8 (both lanes, the
+                        // odd one only, or neither take the polynomial)
+                        constexpr int kFirstPoly = 8 - POLY_PER8;
                         float2 pv;
-                        if ((e & 7) >= 8 - POLY_PER8) {
-                            pv = exp2_poly3_x2(xv);
+                        if ((e & 7) >= kFirstPoly) {
+                            pv = exp2_poly_x2<POLY_DEG>(xv);
+                        } else if (((e + 1) & 7) >= kFirstPoly) {
+                            pv.x = ex2_mufu(xv.x);
+                            pv.y = exp2_poly<POLY_DEG>(xv.y);
                         } else {
                             pv.x = ex2_mufu(xv.x);
                             pv.y = ex2_mufu(xv.y);
@@ -578,10 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
-template <int D, int PG>
+template <int D, int PG, int DEG>
 cudaError_t launch_fwd_inst(const FwdArgs &a, cudaStream_t stream) {
     using Cfg = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, PG>;
+    auto kern = fa_fwd_kernel<D, PG, DEG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -592,13 +601,22 @@ cudaError_t launch_fwd_inst(const FwdArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int D, int DEG>
+cudaError_t launch_fwd_deg(const FwdArgs &a, cudaStream_t stream) {
+    switch (a.poly_groups) {
+        case 1: return launch_fwd_inst<D, 1, DEG>(a, stream);
+        case 2: return launch_fwd_inst<D, 2, DEG>(a, stream);
+        case 8: return launch_fwd_inst<D, 8, DEG>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs &a, cudaStream_t stream) {
-    switch (a.poly_groups) {
-        case 0: return launch_fwd_inst<D, 0>(a, stream);
-        case 1: return launch_fwd_inst<D, 1>(a, stream);
-        case 2: return launch_fwd_inst<D, 2>(a, stream);
-        case 8: return launch_fwd_inst<D, 8>(a, stream);
+    if (a.poly_groups == 0) return launch_fwd_inst<D, 0, 3>(a, stream);  // MUFU only
+    switch (a.poly_degree) {
+        case 3: return launch_fwd_deg<D, 3>(a, stream);
+        case 5: return launch_fwd_deg<D, 5>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

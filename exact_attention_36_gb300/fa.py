@@ -46,7 +46,7 @@ def lib():
         L = ctypes.CDLL(_LIB_PATH)
         vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
-        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]
+        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, i, i, vp]
         L.fa_fwd_varlen.argtypes = [vp] * 6 + [i, i, i, i, i, i, f, vp]
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
@@ -59,6 +59,8 @@ def lib():
         L.fa_bwd_varlen_deterministic.argtypes = [vp] * 13 + [i, i, i, i, i, i, f, vp]
         L.fa_bwd_semaphore_bytes.argtypes = [i, i, i, i]
         L.fa_bwd_semaphore_bytes.restype = ctypes.c_size_t
+        L.fa_bwd_varlen_semaphore_bytes.argtypes = [i, i, i, i, i]
+        L.fa_bwd_varlen_semaphore_bytes.restype = ctypes.c_size_t
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_cuda_error.argtypes = [ctypes.POINTER(i)]
@@ -103,12 +105,13 @@ def _check_bshd(name, t, shape=None):
 
 
 def fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None,
-        rescale_threshold: float = DEFAULT, poly_exp2_groups: int = DEFAULT):
+        rescale_threshold: float = DEFAULT, poly_exp2_groups: int = DEFAULT,
+        poly_exp2_degree: int = DEFAULT):
     """fa_fwd_ex on caller-provided tensors (o, lse written)."""
     B, S, H, D = q.shape
     st = lib().fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, D,
                          int(bool(causal)), float(scale), float(rescale_threshold),
-                         int(poly_exp2_groups), _stream(stream))
+                         int(poly_exp2_groups), int(poly_exp2_degree), _stream(stream))
     _check("fa_fwd", st)
 
 
@@ -179,11 +182,16 @@ def bwd_semaphore_bytes(B: int, H: int, S: int, D: int) -> int:
     return int(lib().fa_bwd_semaphore_bytes(B, H, S, D))
 
 
+def bwd_varlen_semaphore_bytes(B: int, max_seqlen: int, total: int, H: int, D: int) -> int:
+    return int(lib().fa_bwd_varlen_semaphore_bytes(B, max_seqlen, total, H, D))
+
+
 # ---------------------------------------------------------------- tensor API
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
-            rescale_threshold: float = DEFAULT, poly_exp2_groups: int = DEFAULT):
+            rescale_threshold: float = DEFAULT, poly_exp2_groups: int = DEFAULT,
+            poly_exp2_degree: int = DEFAULT):
     """Exact attention forward.  q, k, v: CUDA bf16 [B, S, H, D].
 
     Returns (o bf16 [B, S, H, D], lse fp32 [B, H, S]).
@@ -196,7 +204,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    fwd(q, k, v, o, lse, causal, scale, stream, rescale_threshold, poly_exp2_groups)
+    fwd(q, k, v, o, lse, causal, scale, stream, rescale_threshold, poly_exp2_groups,
+        poly_exp2_degree)
     return o, lse
 
 
@@ -286,8 +295,8 @@ def backward_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: 
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     if deterministic:
         B = cu_seqlens.numel() - 1
-        sem = torch.empty(bwd_semaphore_bytes(B, H, int(max_seqlen), D) // 4, dtype=torch.int32,
-                          device=q.device)
+        sem = torch.empty(bwd_varlen_semaphore_bytes(B, int(max_seqlen), T, H, D) // 4,
+                          dtype=torch.int32, device=q.device)
         bwd_varlen_deterministic(q, k, v, o, dout, lse, dq_acc, delta, sem, dq, dk, dv, cu_seqlens,
                                  max_seqlen, causal, scale, stream)
     else:
@@ -311,7 +320,8 @@ def device_error(clear: bool = True) -> int:
 def exp2_eval(x: torch.Tensor, variant: int, stream=None) -> torch.Tensor:
     """Approximate 2^x on the device (variant 0 kernel polynomial, 1 full-range
     polynomial, 2 MUFU, 3 the kernel polynomial in two-lane form, 4 the
-    degree-5 full-range polynomial)."""
+    degree-5 full-range polynomial, 5 the degree-5 kernel polynomial in
+    two-lane form)."""
     if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
         raise ValueError("x: expected a contiguous CUDA fp32 tensor")
     y = torch.empty_like(x)

@@ -65,7 +65,8 @@ typedef enum {
  * multi-stage shared-memory ring, tcgen05 MMAs into Tensor Memory, two
  * 128-row query tiles per CTA whose softmax ping-pongs with the tensor core,
  * conditional rescale of O ([de] §3), exp2 split between MUFU and a degree-3
- * polynomial ([nl] Methodologie §2), longest-first tile order for causal
+ * or degree-5 polynomial ([nl] Methodologie §2; MUFU only by default, see
+ * fa_fwd_ex), longest-first tile order for causal
  * masks ([hyper]).
  *   q, k, v : bf16 [B,S,H,D] inputs.      o   : bf16 [B,S,H,D] output.
  *   lse     : fp32 [B,H,S] output (natural log of the scaled, masked scores).
@@ -75,7 +76,7 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
 
 /*
  * Forward with explicit numerics knobs (used to test that they do not change
- * the result beyond rounding).
+ * the result beyond rounding, and to measure the exp2 split).
  *   rescale_threshold : the running maximum (log2 units) may grow by this
  *                       much before O and the row sum are rescaled; 0 means
  *                       rescale whenever the maximum grows ([de] §3).
@@ -84,11 +85,16 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *                       exp2 from the FMA polynomial instead of MUFU ([nl]
  *                       Methodologie §2): one of 0 (MUFU only), 1 (12.5 %),
  *                       2 (25 %), 8 (polynomial only); -1 selects the
- *                       library default.
+ *                       library default (0).
+ *   poly_exp2_degree  : degree of that polynomial, 3 or 5 ([nl] Methodologie
+ *                       §2: "degree 3 or 5"); -1 selects the default (3).
+ *                       Ignored when poly_exp2_groups is 0.
+ * Other values of a knob give FA_ERR_INVALID_ARG.
  */
 fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                     int B, int H, int S, int D, int causal, float scale,
-                    float rescale_threshold, int poly_exp2_groups, void *stream);
+                    float rescale_threshold, int poly_exp2_groups, int poly_exp2_degree,
+                    void *stream);
 
 /*
  * Forward over a packed batch of sequences of different lengths (prefill
@@ -177,18 +183,21 @@ fa_status fa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
  * results as fa_bwd to rounding, except that every element of dQ is summed
  * over the key tiles in an order fixed by (B, H, S, causal) and the device's
  * SM count, so repeated calls on the same inputs on the same GPU model give
- * bitwise-identical dQ, dK and dV.  Each 128-query block has a counter; the
- * key tile whose turn it is adds its share.  Without a causal mask the order
- * puts the tiles that run at the same time one step apart; with one, the
- * tiles are taken in the order they reach the block in the persistent
- * schedule (one step per block), so few of them wait.  The kernel is
- * launched cooperatively, so all its CTAs are resident while they wait on one
- * another.
- *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes: the
- *            counters, then the order keys of the key tiles (contents on
- *            entry ignored; the first launch writes both).
+ * bitwise-identical dQ, dK and dV.  Each 128-query block has a place for
+ * every key tile that reaches it; without a causal mask the order puts the
+ * tiles that run at the same time one step apart, with one it follows the
+ * order in which the tiles reach the block in the persistent schedule (one
+ * step per block).  At D = 64 and 128 the places alternate between two fp32
+ * accumulators (so consecutive tiles do not wait on each other), each summed
+ * in its fixed order under a counter, and the two are added in a fixed order
+ * at the end.  The kernel is launched cooperatively, so all its CTAs are
+ * resident while they wait on one another.
+ *   dq_sem : scratch of fa_bwd_semaphore_bytes(B,H,S,D) bytes, 16-byte
+ *            aligned: the counters, the order keys of the key tiles and (D =
+ *            64, 128) the second accumulator (contents on entry ignored; the
+ *            first launch initialises all three).
  * At D = 256 (a work unit is a key tile and one half of the head dim) the
- * key tiles take their turns in ascending order per half.
+ * key tiles take their turns in ascending order per half, in one accumulator.
  * Other arguments, results and errors as fa_bwd.
  */
 size_t fa_bwd_semaphore_bytes(int B, int H, int S, int D);
@@ -201,9 +210,11 @@ fa_status fa_bwd_deterministic(const void *q, const void *k, const void *v, cons
  * fa_bwd_deterministic over a packed batch (arguments as fa_bwd_varlen, plus
  * dq_sem): every sequence's dQ is summed over its key tiles in a fixed order,
  * so repeated calls give bitwise-identical dQ, dK and dV.
- *   dq_sem : int scratch of fa_bwd_semaphore_bytes(B, H, max_seqlen, D) bytes
- *            (B = number of sequences), 16-byte aligned, contents ignored.
+ *   dq_sem : scratch of fa_bwd_varlen_semaphore_bytes(B, max_seqlen, total,
+ *            H, D) bytes (B = number of sequences), 16-byte aligned, contents
+ *            ignored.  The size function returns 0 for invalid sizes.
  */
+size_t fa_bwd_varlen_semaphore_bytes(int B, int max_seqlen, int total, int H, int D);
 fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *v, const void *o,
                                       const void *dout, const float *lse, float *dq_acc,
                                       float *delta, int *dq_sem, void *dq, void *dk, void *dv,
@@ -221,8 +232,10 @@ fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *
  * scratch comes from one fixed array of 72 MiB inside the library, held on
  * every GPU that loads the library until the process exits.  Problems whose
  * scratch (fa_bwd_workspace_size) exceeds 72 MiB are rejected with
- * FA_ERR_INVALID_ARG.  The first call on each device looks up the array's
- * device address (make it before any stream capture).  All calls on a
+ * FA_ERR_INVALID_ARG.  The first call on each device, and the first call
+ * after that device's context was replaced (cudaDeviceReset), looks up the
+ * array's device address (make those calls before any stream capture).  All
+ * calls on a
  * device share the array: calls whose kernels may overlap on the GPU race
  * and must be serialised by the caller.  Each call re-zeroes the part of the
  * scratch it uses, so nothing carries over between calls.  Allocates nothing.
@@ -259,7 +272,9 @@ fa_status fa_device_error(int *code, int clear);
  *   variant 3 = the kernel polynomial in its two-lane (f32x2) form, as the
  *               softmax evaluates it (same range and clamp as variant 0),
  *   variant 4 = the degree-5 polynomial ([nl] Methodologie §2: degree 3 or
- *               5) with exact subnormal scaling, like variant 1.
+ *               5) with exact subnormal scaling, like variant 1,
+ *   variant 5 = the degree-5 polynomial in the two-lane form the softmax
+ *               evaluates (range and clamp of variant 0).
  * fa_exp2_sweep: every fp32 x with lo <= x <= hi (lo, hi finite, lo <= hi)
  *   is evaluated with `variant` and compared to 2^x in double precision;
  *   the largest relative error |y - 2^x| / max(2^x, 2^-126) and its

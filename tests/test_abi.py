@@ -65,10 +65,13 @@ def test_argument_errors_need_no_device(lib):
     # unsupported head dim
     assert lib.fa_fwd(p, p, p, p, p, 1, 1, 128, 96, 0, 0.1, null) == fa.FA_ERR_UNSUPPORTED
     # knobs out of range
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, 17.0, 0, null) == \
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, 17.0, 0, -1, null) == \
         fa.FA_ERR_INVALID_ARG
-    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, 8.0, 3, null) == \
+    assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, 8.0, 3, -1, null) == \
         fa.FA_ERR_INVALID_ARG
+    for deg in (0, 1, 2, 4, 6, 7):  # the polynomial's degree is 3 or 5
+        assert lib.fa_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, 8.0, 1, deg, null) == \
+            fa.FA_ERR_INVALID_ARG
     ptrs = [p] * 11
     ptrs[6] = null
     assert lib.fa_bwd(*ptrs, 1, 1, 128, 64, 0, 0.1, null) == fa.FA_ERR_INVALID_ARG
@@ -82,7 +85,7 @@ def test_argument_errors_need_no_device(lib):
         assert lib.fa_bwd_ex(*ok, 1, 1, 128, D, 0, 0.1, 1, null) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_exp2_sweep(1.0, 0.0, 0, p, null) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_exp2_eval(p, p, -1, 0, null) == fa.FA_ERR_INVALID_ARG
-    assert lib.fa_exp2_eval(p, p, 16, 5, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_exp2_eval(p, p, 16, 6, null) == fa.FA_ERR_INVALID_ARG
 
 
 def test_workspace_size(lib):
@@ -95,18 +98,29 @@ def test_workspace_size(lib):
 
 
 def test_semaphore_and_varlen_scratch_sizes(lib):
-    # fixed-order mode: counters per 64 query rows, then one order key per
-    # 128-key tile, each part padded to 256 bytes
+    # fixed-order mode at D = 64/128: per 128-query block one counter per
+    # drain warp and accumulator (4 x 2), one order key per 128-key tile, then
+    # the second fp32 accumulator; each part padded to 256 bytes
+    def pad(x):
+        return (x + 255) // 256 * 256
+
     B, H, S, D = 2, 3, 1000, 128
-    counters = B * H * ((S + 63) // 64)
-    keys = B * H * ((S + 127) // 128)
-    want = (counters * 4 + 255) // 256 * 256 + (keys * 4 + 255) // 256 * 256
+    nT = (S + 127) // 128
+    want = pad(B * H * 8 * nT * 4) + pad(B * H * nT * 4) + pad(B * H * S * D * 4)
     assert lib.fa_bwd_semaphore_bytes(B, H, S, D) == want
     assert lib.fa_bwd_semaphore_bytes(B, H, 0, D) == 0
-    # D = 256: one set of counters per half of the head dim, no order keys
-    assert lib.fa_bwd_semaphore_bytes(B, H, S, 256) == 2 * ((counters * 4 + 255) // 256 * 256)
+    # D = 256: one counter per 64 query rows, half of the head dim and drain warp
+    assert lib.fa_bwd_semaphore_bytes(B, H, S, 256) == pad(B * H * 8 * ((S + 63) // 64) * 4)
+    # packed batches: counters and keys per sequence and the longest one's
+    # tiles, the second accumulator over all tokens
+    T, Bs, L = 1234, 5, 700
+    nT = (L + 127) // 128
+    want = pad(Bs * H * 8 * nT * 4) + pad(Bs * H * nT * 4) + pad(H * T * D * 4)
+    assert lib.fa_bwd_varlen_semaphore_bytes(Bs, L, T, H, D) == want
+    assert lib.fa_bwd_varlen_semaphore_bytes(Bs, L, T, H, 256) == \
+        pad(Bs * H * 8 * ((L + 63) // 64) * 4)
+    assert lib.fa_bwd_varlen_semaphore_bytes(Bs, T + 1, T, H, D) == 0
     # packed batches: the accumulator and Delta over all tokens, as fa_bwd's
-    T = 1234
     assert lib.fa_bwd_varlen_workspace_size(T, H, D) == lib.fa_bwd_workspace_size(1, H, T, D)
 
 

@@ -54,13 +54,20 @@ def test_degree5_polynomial_exhaustive_minus127_to_0():
     assert err <= 1e-6
 
 
+def test_degree5_kernel_form_on_its_range():
+    # the two-lane degree-5 form the softmax instances evaluate (clamp at -125)
+    err, x = fa.exp2_sweep(-125.0, 16.0, variant=5)
+    assert err <= GATE, (err, x)
+    assert err <= 1e-6
+
+
 def test_mufu_reference_range():
     err, x = fa.exp2_sweep(-126.0, 16.0, variant=2)
     assert err <= 2.0 ** -20, (err, x)
 
 
 @pytest.mark.parametrize("variant,lo,hi", [(1, -127.0, 0.0), (0, -125.0, 16.0), (2, -126.0, 16.0),
-                                            (4, -127.0, 0.0)])
+                                            (4, -127.0, 0.0), (5, -125.0, 16.0)])
 def test_sampled_against_oracle_exp2(variant, lo, hi):
     g = torch.Generator().manual_seed(variant)
     x = lo + (hi - lo) * torch.rand(1 << 20, generator=g, dtype=torch.float64)

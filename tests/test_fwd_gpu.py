@@ -72,7 +72,7 @@ def test_stress_sweep(S, B, D, causal):
     q, k, v, o, lse, scale = _run(B, 16, S, D, causal, stress=True)
     rows = None if S <= 4096 else sample_rows(S, 128, seed=2)
     check_forward(q, k, v, o, lse, causal, scale, heads=[(0, 0), (B - 1, 15)], rows=rows,
-                  peaked=True)
+                  peaked=True, case=f"B{B}_H16_S{S}_D{D}_{'causal' if causal else 'noncausal'}")
 
 
 @pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
@@ -89,11 +89,45 @@ def test_numerics_knobs_do_not_change_result(tau, groups):
     assert (lse - lse_ref).abs().max().item() <= 1e-3
 
 
+@pytest.mark.parametrize("degree", [3, 5])
+@pytest.mark.parametrize("groups", [1, 2, 8])
+def test_polynomial_columns_are_taken(groups, degree):
+    # the split really moves exponentials to the polynomial: its values differ
+    # from MUFU's in the last bits, so the row sums (fp32, before the bf16
+    # rounding of P) and hence some LSE values differ from the MUFU-only run
+    q, k, v, _ = make_qkvdo(1, 4, 512, 128, seed=13, with_dout=False)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    _, lse0 = fa.forward(qd, kd, vd, poly_exp2_groups=0)
+    _, lse1 = fa.forward(qd, kd, vd, poly_exp2_groups=groups, poly_exp2_degree=degree)
+    torch.cuda.synchronize()
+    assert not torch.equal(lse0, lse1)
+    assert (lse0 - lse1).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("groups", [1, 2, 8])
+def test_degree5_polynomial_instances(D, groups):
+    # the pages allow a polynomial of degree 3 or 5: the degree-5 instances
+    # against the oracle, and against the MUFU-only result of the same inputs
+    q, k, v, o, lse, scale = _run(2, 4, 1024, D, True, stress=True, poly_exp2_groups=groups,
+                                  poly_exp2_degree=5)
+    check_forward(q, k, v, o, lse, True, scale, heads=[(0, 0), (1, 3)], peaked=True)
+    _, _, _, o_ref, lse_ref, _ = _run(2, 4, 1024, D, True, stress=True, poly_exp2_groups=0)
+    assert (o.float() - o_ref.float()).abs().max().item() <= 2e-2
+    assert (lse - lse_ref).abs().max().item() <= 1e-3
+    # with every exponential on the degree-5 polynomial (relative error ~2e-7
+    # against MUFU's ~2^-22) the non-peaked inputs match the oracle as closely
+    # as the MUFU path does
+    q, k, v, o, lse, scale = _run(1, 3, 700, D, False, seed=5, poly_exp2_groups=groups,
+                                  poly_exp2_degree=5)
+    check_forward(q, k, v, o, lse, False, scale, heads=None)
+
+
 @pytest.mark.parametrize("D", [64, 256])
-@pytest.mark.parametrize("groups", [0, 2])
-def test_numerics_knobs_other_head_dims(D, groups):
+@pytest.mark.parametrize("groups,degree", [(0, 3), (2, 3), (2, 5)])
+def test_numerics_knobs_other_head_dims(D, groups, degree):
     q, k, v, o, lse, scale = _run(1, 3, 700, D, True, stress=True, rescale_threshold=0.0,
-                                  poly_exp2_groups=groups)
+                                  poly_exp2_groups=groups, poly_exp2_degree=degree)
     check_forward(q, k, v, o, lse, True, scale, heads=None, peaked=True)
 
 
@@ -110,3 +144,5 @@ def test_rejects_bad_arguments():
     with pytest.raises(fa.FAError, match="UNSUPPORTED"):
         x = torch.zeros(1, 128, 1, 96, dtype=torch.bfloat16, device="cuda")
         fa.forward(x, x, x)
+    with pytest.raises(fa.FAError, match="INVALID_ARG"):
+        fa.forward(q, q, q, poly_exp2_groups=1, poly_exp2_degree=4)

@@ -11,12 +11,16 @@
 //
 // The array lives in device global memory of every GPU that loads this
 // library and stays there until the process exits.  Its address is looked up
-// once per device, on the first call made with that device current; make
-// that first call before capturing any stream.  All calls on a device share
-// the array, so two calls whose kernels overlap on that GPU (for example on
-// two streams) race on it and must be serialised by the caller.  The
-// backward's first kernel zeroes the part of the accumulator a call uses and
-// rewrites Delta, so nothing is carried over from an earlier call.
+// on the first call made with a device current, and again on the first call
+// after that device's context was replaced (cudaDeviceReset reloads the
+// module, which can move the array); make those calls before capturing any
+// stream.  All calls on a device share the array, so two calls whose kernels
+// overlap on that GPU (for example on two streams) race on it and must be
+// serialised by the caller.  The backward's first kernel zeroes the part of
+// the accumulator a call uses and rewrites Delta, so nothing is carried over
+// from an earlier call.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "fa.h"
@@ -30,23 +34,59 @@ constexpr size_t kScratchBytes = size_t(72) << 20;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchSlot {
+    unsigned long long ctx_id = 0;  // unique id of the context the address belongs to
+    void *addr = nullptr;
+};
+ScratchSlot g_scratch[kMaxDevices];
 std::mutex g_scratch_mutex;
 
-// Device address of g_bwd_scratch on the current device (set up once per
-// device).  In host code the symbol's name is only a stand-in: the address
-// the kernels need comes from cudaGetSymbolAddress.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Unique id of the calling thread's current context (0 if none yet).
+unsigned long long current_ctx_id() {
+    std::call_once(g_ctx_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+    });
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_bwd_scratch on the current device.  In host code the
+// symbol's name is only a stand-in: the address the kernels need comes from
+// cudaGetSymbolAddress, looked up once per device and context.
 fa_status scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchSlot &slot = g_scratch[dev];
+    const unsigned long long id = current_ctx_id();
+    if (!slot.addr || id == 0 || id != slot.ctx_id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return FA_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        slot.addr = p;
+        // the lookup made the device's context current if it was not yet
+        slot.ctx_id = id ? id : current_ctx_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return FA_OK;
 }
 

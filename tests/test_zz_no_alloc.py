@@ -32,10 +32,13 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row(causal):
+def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row(causal, D):
+    # every head dim: D = 256 reaches the array through its own main kernel
+    # (dQ^T reduced over 64-row blocks with its own accumulator map)
     fn = _noalloc_fn()
-    B, H, S, D = 2, 4, 1000, 128
+    B, H, S = (2, 4, 1000) if D != 256 else (1, 4, 1000)
     scale = 1.0 / math.sqrt(D)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for seed in (21, 22):

@@ -302,6 +302,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     if ((st = make_map_bshd(&a.tm_q, q, mb, ms, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_k, k, mb, ms, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_v, v, mb, ms, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_o, o, mb, ms, H, D)) != FA_OK) return st;
     a.o = o;
     a.lse = lse;
     a.B = B;
@@ -371,14 +372,15 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     if (cu && (B < 1 || S < 1 || S > T || (reinterpret_cast<uintptr_t>(cu) & 3u)))
         return FA_ERR_INVALID_ARG;
     if (pair_mode < -1 || pair_mode > 1) return FA_ERR_INVALID_ARG;
-    // packed batches: the single-CTA kernel (D = 64, 128), atomic-order dQ
-    if (cu && pair_mode == 1) return FA_ERR_UNSUPPORTED;
-    // CTA pairs: D = 128 with atomic-order dQ only.  Not the default: on
-    // GB300 the single-CTA kernel is faster (the pair's dQ MMA, M = 128 over
-    // two SMs, runs at half the per-SM tensor rate, and the dS exchange adds
-    // latency to the block chain)
+    // CTA pairs: fixed-length batches with atomic-order dQ, D = 128 or 256.
+    // Not the default: on GB300 the single-CTA kernels are faster.  D = 128:
+    // the pair's dQ MMA (M = 128 over two SMs) runs at half the per-SM tensor
+    // rate, and the dS exchange adds latency to the block chain.  D = 256: the
+    // pair splits the work by role and computes nothing twice, but each block
+    // waits for a round trip of P^T and dS^T between the two SMs (measured
+    // 498 / 489 TFLOPS against 591 / 548 at S = 16384).
+    if (pair_mode == 1 && (cu || sem || D == 64)) return FA_ERR_UNSUPPORTED;
     const bool pair = pair_mode == 1;
-    if (pair && (D != 128 || sem)) return FA_ERR_UNSUPPORTED;
     const DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != FA_OK) return st;
     if ((st = get_encoder()) != FA_OK) return st;
@@ -394,7 +396,10 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     if ((st = make_map_bshd(&a.tm_v, v, mb, ms, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_do, dout, mb, ms, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, mb * H, ms, D, dqrows)) != FA_OK) return st;
-    if (pair) {
+    if (pair && D == 256) {
+        if ((st = make_map_dqacc(&a.tm_dqacc16, dq_acc, mb * H, ms, D, 16)) != FA_OK) return st;
+    }
+    if (pair && D == 128) {
         if ((st = make_map_bshd(&a.tm_q64, q, B, S, H, D, 64)) != FA_OK) return st;
         if ((st = make_map_bshd(&a.tm_do64, dout, B, S, H, D, 64)) != FA_OK) return st;
     }

@@ -19,6 +19,7 @@ enum DeviceError : int {
 
 struct FwdArgs {
     CUtensorMap tm_q, tm_k, tm_v;  // bf16 [B,S,H,D], box 64 x 1 x 128 x 1, 128B swizzle
+    CUtensorMap tm_o;              // the output, same geometry (TMA-store epilogue)
     void *o;                       // bf16 [B,S,H,D]
     float *lse;                    // fp32 [B,H,S]
     int B, H, S, D;
@@ -36,6 +37,7 @@ struct FwdArgs {
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [B,S,H,D], same boxes as the forward
     CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 32 x 1
+    CUtensorMap tm_dqacc16;               // D = 256 on CTA pairs: the same, box 32 x 16 x 1
     CUtensorMap tm_q64, tm_do64;          // CTA pairs: Q and dO with 64-row boxes
     const void *o, *dout;                 // bf16 [B,S,H,D]
     const float *lse;                     // fp32 [B,H,S]
@@ -57,7 +59,7 @@ struct BwdArgs {
     float scale_log2;
     int *err_word;
     int num_sms;
-    int pair;                             // 1: D = 128 main kernel on CTA pairs
+    int pair;                             // 1: main kernel on CTA pairs (D = 128, 256)
     const int *cu_seqlens;                // packed variable-length batch, else null
     int T;                                // packed: total tokens (S = longest sequence)
 };
@@ -112,5 +114,9 @@ cudaError_t launch_bwd_main_d256(const BwdArgs &a, cudaStream_t stream);
 // main backward kernel for D = 128 on CTA pairs (fa_bwd_pair.cu); Q/dO maps
 // with 128- and 64-row boxes and a dQ-accumulator map with 32 x 64 boxes
 cudaError_t launch_bwd_main_pair(const BwdArgs &a, cudaStream_t stream);
+// main backward kernel for D = 256 on CTA pairs split by role
+// (fa_bwd_d256_split.cu); fixed-length batches, atomic-order dQ; maps as for
+// launch_bwd_main_d256
+cudaError_t launch_bwd_main_d256_split(const BwdArgs &a, cudaStream_t stream);
 
 }  // namespace fa

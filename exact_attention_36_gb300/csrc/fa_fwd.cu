@@ -66,9 +66,16 @@ struct FwdCfg {
     static constexpr int kGroups = kStages / 2;
     static constexpr int kQBytes = kNQ * kTileBytes;
     static constexpr int kRingOff = kQBytes;
-    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain
-    static constexpr int kNumBars = 2 + 2 * kStages + 7;
+    // Epilogue staging: O of a finished tile is written here (bf16, in the
+    // TMA box layout) and stored by TMA.  D = 64: one buffer per query tile;
+    // D = 128: one buffer the two tiles take in turn (shared memory has room
+    // for one beside Q and the ring); D = 256: none (direct stores).
+    static constexpr int kStageBufs = (D == 64) ? 2 : (D == 128 ? 1 : 0);
+    static constexpr int kStageOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kStageOff + kStageBufs * kTileBytes;
+    // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain,
+    // stage_free[2], staged[2]
+    static constexpr int kNumBars = 2 + 2 * kStages + 11;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -144,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint64_t *p_full = s_full + 2;
     uint64_t *o_full = s_full + 4;
     uint64_t *drain = s_full + 6;
+    uint64_t *stage_free = s_full + 7;  // [2]: a staging buffer's TMA store has read it
+    uint64_t *staged = s_full + 9;      // [2]: the four warps of a tile wrote its O rows
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
 
@@ -167,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_init(&o_full[t], 1);
         }
         mbar_init(drain, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&stage_free[t], 1);
+            mbar_init(&staged[t], 4);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -313,6 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     mma_commit(&s_full[0]);
                     issue_qk<D>(tS1, q1, kaddr);
                     mma_commit(&s_full[1]);
+                    // Q is read only by the S MMAs: once the unit's last one is
+                    // issued, the next unit's Q may load (its latency then
+                    // overlaps this unit's last key tile and epilogue)
+                    if (n1 == 1) mma_commit(q_empty);
                     for (int j = 0; j < n1; ++j) {
                         g = ring % Cfg::kGroups;
                         w.code = kErrFwdWait + 12;
@@ -341,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         if (j + 1 < n1) {
                             issue_qk<D>(tS1, q1, kaddr);
                             mma_commit(&s_full[1]);
+                            if (j + 2 == n1) mma_commit(q_empty);  // the last S MMA
                         } else {
                             mma_commit(&o_full[1]);
-                            mma_commit(q_empty);
                         }
                     }
                 } else {
@@ -360,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         mma_commit(&s_full[1]);
                     }
                     mma_commit(&kv_empty[kslot]);
+                    // Q is read only by the S MMAs (see the grouped path)
+                    if (n1 == 1) mma_commit(q_empty);
                     for (int j = 0; j < n1; ++j) {
                         const uint32_t vslot = ring % Cfg::kStages;
                         w.code = kErrFwdWait + 12;
@@ -389,10 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                                 tc_fence_after();
                                 issue_qk<D>(tS0, q0, naddr);
                                 mma_commit(&s_full[0]);
-                                if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[nslot]);
+                                if constexpr (Cfg::kNQ == 1) {
+                                    mma_commit(&kv_empty[nslot]);
+                                    if (j + 2 == n0) mma_commit(q_empty);  // the last S MMA
+                                }
                             } else {
                                 mma_commit(&o_full[0]);
-                                if constexpr (Cfg::kNQ == 1) mma_commit(q_empty);
                             }
                         }
                         if constexpr (Cfg::kNQ == 1) continue;
@@ -411,9 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                             issue_qk<D>(tS1, q1, naddr);
                             mma_commit(&s_full[1]);
                             mma_commit(&kv_empty[nslot]);
+                            if (j + 2 == n1) mma_commit(q_empty);  // the last S MMA
                         } else {
                             mma_commit(&o_full[1]);
-                            mma_commit(q_empty);
                         }
                     }
                 }
@@ -555,30 +576,92 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             oph ^= 1;
             tc_fence_after();
             const float inv_l = 1.f / l;
+            const int tile_row0 = un.p * Cfg::kRows + t * kBlockM;
             uint16_t *orow = reinterpret_cast<uint16_t *>(args.o) +
                              ((static_cast<size_t>(sp.tok0) + row) * H + h) * D;
+            if constexpr (Cfg::kStageBufs > 0) {
+                // O goes through a shared-memory tile in the TMA box layout and
+                // leaves in one TMA store per 64 columns (16-byte shared stores
+                // instead of 16-byte global stores 4 KB apart).  The k-th use of
+                // a buffer waits for the (k-1)-th release (parity (k & 1) ^ 1).
+                // D = 64: one buffer per tile, k = this tile's unit count, whose
+                // parity oph now holds (k + 1); D = 128: the tiles take the one
+                // buffer in turn, k = 2u + t, so the parity is t's.
+                const int buf = (Cfg::kStageBufs == 2) ? t : 0;
+                const uint32_t use_par = (Cfg::kStageBufs == 2) ? (oph ^ 1) : static_cast<uint32_t>(t);
+                // a packed batch's last tile of a sequence would overwrite the
+                // next sequence's rows: that tile keeps direct stores
+                const bool use_tma = !args.cu_seqlens || tile_row0 + kBlockM <= len;
+                if (!mbar_wait(&stage_free[buf], use_par ^ 1, w)) { ok = false; break; }
+                uint8_t *stg = smem + Cfg::kStageOff + buf * Cfg::kTileBytes;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t orr[32];
-                tmem_ld32(tO + c * 32, orr);
-                tmem_ld_wait(orr);
-                uint32_t pk[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + c * 32, orr);
+                    tmem_ld_wait(orr);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                                        __uint_as_float(orr[2 * e + 1]) * inv_l);
-                if (row < len) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                                            __uint_as_float(orr[2 * e + 1]) * inv_l);
+                    if (use_tma) {
+                        // row r_in_tile of box c/2: 16-byte chunks (c%2)*4 + v4,
+                        // 128B swizzle (chunk index xor row % 8)
+                        uint8_t *srow = stg + (c >> 1) * kBox + r_in_tile * 128;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                             pk[4 * v4 + 3]);
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            *reinterpret_cast<uint4 *>(
+                                srow + ((((c & 1) * 4 + v4) ^ (r_in_tile & 7)) << 4)) =
+                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                           pk[4 * v4 + 3]);
+                    } else if (row < len) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                 pk[4 * v4 + 3]);
+                    }
+                }
+                if (use_tma) fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&staged[buf]);
+                if (r_in_tile == 0) {  // the tile's TMA stores of O
+                    if (!mbar_wait(&staged[buf], use_par, w)) { ok = false; break; }
+                    if (use_tma) {
+#pragma unroll
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_store_4d(&args.tm_o, stg + c * kBox, 64 * c, h,
+                                         sp.trow0 + tile_row0, sp.tb);
+                        bulk_commit();
+                        bulk_wait_read<0>();  // the buffer has been read
+                    }
+                    mbar_arrive(&stage_free[buf]);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + c * 32, orr);
+                    tmem_ld_wait(orr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                                            __uint_as_float(orr[2 * e + 1]) * inv_l);
+                    if (row < len) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                 pk[4 * v4 + 3]);
+                    }
                 }
             }
             if (row < len)
                 args.lse[stat_index(args.cu_seqlens, args.T, S, H, b, h, sp, row)] =
                     (m_used + log2f(l)) * 0.69314718055994531f;
         }
+        if (Cfg::kStageBufs > 0 && r_in_tile == 0) bulk_wait<0>();  // its O stores are complete
     }
 
     tc_fence_before();
@@ -590,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 template <int D, int PG, int DEG>
 cudaError_t launch_fwd_inst(const FwdArgs &a, cudaStream_t stream) {
     using Cfg = FwdCfg<D>;
+    static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
     auto kern = fa_fwd_kernel<D, PG, DEG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);

@@ -179,6 +179,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, const 
         "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// 4-D tiled store shared -> global, tracked by this thread's bulk
+// async-groups.  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *smem_src, int c0,
+                                             int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+        " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -392,6 +402,54 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 // release costs about 1300 cycles per arrive.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+// Arrive on a cluster mbarrier with release at cluster scope: orders this
+// thread's earlier writes (and, through a preceding __syncwarp, its warp's)
+// to the other CTA's shared memory before the arrival.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+                 : "memory");
+}
+// Arrive on a cluster mbarrier and add `bytes` to the transaction count its
+// current phase waits for (the bytes of a bulk copy that will complete on it).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cl_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cl_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+// Wait for a phase of a local mbarrier whose arrivals carry cluster-scope
+// releases (data written by the other CTA of the cluster): acquire at cluster
+// scope.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > FA_WAIT_LIMIT_NS) {
+            *w.abort_flag = 1;
+            atomicCAS(w.err_word, 0, w.code);
+            return false;
+        }
+    }
+}
+// 16-byte store to shared memory anywhere in the cluster (address from mapa_shared).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cl_addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cl_addr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
 // shared memory anywhere in the cluster; completion (bytes) is counted on the

@@ -19,8 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_d256.cu", "fa_bwd_pair.cu",
-           "fa_bwd_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_d256.cu", "fa_bwd_d256_split.cu",
+           "fa_bwd_pair.cu", "fa_bwd_noalloc.cu"]
 
 
 def _nvcc() -> str:

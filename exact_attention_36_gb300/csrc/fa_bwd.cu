@@ -1012,7 +1012,9 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
             fa_bwd_prep<256><<<blocks, 256, 0, stream>>>(rows_view);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
-            if ((e = launch_bwd_main_d256(a, stream)) != cudaSuccess) return e;
+            if ((e = a.pair ? launch_bwd_main_d256_split(a, stream) : launch_bwd_main_d256(a, stream)) !=
+                cudaSuccess)
+                return e;
             fa_bwd_dq_cvt<256><<<blocks, 256, 0, stream>>>(rows_view);
             return cudaGetLastError();
         }

@@ -160,14 +160,21 @@ fa_status fa_bwd_varlen(const void *q, const void *k, const void *v, const void 
  * Backward with the choice of main kernel ([nl] Methodologie §3: the 2-CTA
  * MMA mode splits operand B between two CTAs, and the pair exchanges halves
  * of the dQ work through distributed shared memory).
- *   pair_mode : 0  one CTA per 128-key tile (every head dimension);
- *               1  CTA pairs: two neighbouring SMs own two adjacent key tiles
+ *   pair_mode : 0  one CTA per 128-key tile (every head dimension; at
+ *                  D = 256 a CTA per key tile and half of the head dim, which
+ *                  computes S^T and dP^T for both halves);
+ *               1  CTA pairs (fixed-length batches, atomic-order dQ):
+ *                  D = 128: two neighbouring SMs own two adjacent key tiles
  *                  and issue their MMAs together (tcgen05 .cta_group::2);
  *                  each CTA stages half of every Q/dO operand the MMAs read
- *                  and reduces only half of the dQ rows.  D = 128 only
- *                  (other D: FA_ERR_UNSUPPORTED);
- *              -1  library default (0: on GB300 the pair kernel measures
- *                  slower, see the kernel's source).
+ *                  and reduces only half of the dQ rows.
+ *                  D = 256: two neighbouring SMs share one key tile and split
+ *                  the work by role: one forms P^T, dV and half of dQ, the
+ *                  other dP^T, dS^T, dK and the other half of dQ; P^T and dS^T
+ *                  cross between them through distributed shared memory.
+ *                  D = 64: FA_ERR_UNSUPPORTED;
+ *              -1  library default (0: on GB300 both pair kernels measure
+ *                  slower than the single-CTA ones, see their sources).
  * Other arguments, results and errors as fa_bwd; the results agree with
  * pair_mode 0 to rounding (fp32 operations in a different order).
  */

@@ -81,8 +81,8 @@ def test_argument_errors_need_no_device(lib):
         [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
     for mode in (-2, 2):
         assert lib.fa_bwd_ex(*ok, 1, 1, 128, 128, 0, 0.1, mode, null) == fa.FA_ERR_INVALID_ARG
-    for D in (64, 256):
-        assert lib.fa_bwd_ex(*ok, 1, 1, 128, D, 0, 0.1, 1, null) == fa.FA_ERR_UNSUPPORTED
+    # CTA pairs exist for D = 128 and 256
+    assert lib.fa_bwd_ex(*ok, 1, 1, 128, 64, 0, 0.1, 1, null) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_exp2_sweep(1.0, 0.0, 0, p, null) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_exp2_eval(p, p, -1, 0, null) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_exp2_eval(p, p, 16, 6, null) == fa.FA_ERR_INVALID_ARG

@@ -100,15 +100,14 @@ struct BUnit {
     int j;   // key tile; -1 = no unit for this CTA this round
 };
 
-// Unit u -> (bh, key tile).  By default the key tiles of one head are
+// Unit u -> (bh, key tile).  Without a mask the key tiles of one head are
 // consecutive (concurrent CTAs share that head's Q, dO and dQ accumulator in
-// L2), key tile 0 first.  The fixed-order mode under a causal mask, where tile
-// j has nT - j query blocks and a CTA that runs long holds up the tiles
-// waiting on it, numbers the units tile-major instead (every head's tile 0,
-// then tile 1, ...): with the serpentine rounds that is a longest-first order
-// across heads, which balances the CTAs (572 -> 659 TFLOPS at S = 32768).  The
-// atomic-order kernel keeps the head-major order: tile-major measured +1.5 %
-// causal there but cost 1.2 % without a mask through code generation.
+// L2), key tile 0 first.  Under a causal mask tile j has nT - j query blocks,
+// and the units are numbered tile-major instead (every head's tile 0, then
+// tile 1, ...): with the serpentine rounds that is a longest-first order
+// across heads, which balances the CTAs (head by head, the busiest CTA runs
+// about 10 % more blocks than the average at S = 32768, H = 16; the
+// fixed-order mode went from 572 to 659 TFLOPS).
 __device__ __forceinline__ void unit_coords(int u, int nT, int BH, bool causal, int &bh, int &j) {
     if (causal) {
         j = u / BH;
@@ -296,8 +295,10 @@ __device__ __forceinline__ void issue_dk(uint32_t tAcc, uint32_t ds_saddr, uint3
 // ---------------------------------------------------------------- main kernel
 
 // kDet: the fixed-order dQ mode (args.dq_sem set), a separate instance so
-// that the atomic-order kernel carries none of its logic
-template <int D, bool kDet>
+// that the atomic-order kernel carries none of its logic.  kTileMajor: units
+// numbered tile-major (unit_coords), the order for causal masks, also a
+// separate instance so that the order without a mask keeps its code
+template <int D, bool kDet, bool kTileMajor>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdArgs args) {
     using Cfg = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         const float inv_scale = 1.f / args.scale;
         for (int it = 0; ok; ++it) {
             BUnit un;
-            if (!bunit_at(it, U, BH, kDet && args.causal != 0, un)) break;
+            if (!bunit_at(it, U, BH, kTileMajor, un)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     } while (0)
             for (int it = 0; ok; ++it) {
                 BUnit un;
-                if (!bunit_at(it, U, BH, kDet && args.causal != 0, un)) break;
+                if (!bunit_at(it, U, BH, kTileMajor, un)) break;
                 if (un.j < 0) continue;
                 const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
                 if (un.j * kBlk >= sp.len) continue;
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         const int sw = kr & 7;  // 128B swizzle phase of this row
         for (int it = 0; ok; ++it) {
             BUnit un;
-            if (!bunit_at(it, U, BH, kDet && args.causal != 0, un)) break;
+            if (!bunit_at(it, U, BH, kTileMajor, un)) break;
             if (un.j < 0) continue;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
             if (un.j * kBlk >= sp.len) continue;
@@ -729,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         bool ok = true;
         for (int it = 0; ok; ++it) {
             BUnit un;
-            if (!bunit_at(it, U, BH, kDet && args.causal != 0, un)) break;
+            if (!bunit_at(it, U, BH, kTileMajor, un)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
@@ -975,7 +976,11 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
         fa_bwd_dq_cvt<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(rows_view);
         return cudaGetLastError();
     }
-    auto kern = a.dq_sem ? fa_bwd_kernel<D, true> : fa_bwd_kernel<D, false>;
+    // causal masks: units tile-major, i.e. longest first across heads (head
+    // by head, the serpentine rounds leave the busiest CTA about 10 % more
+    // blocks than the average at S = 32768, H = 16)
+    auto kern = a.dq_sem ? (a.causal ? fa_bwd_kernel<D, true, true> : fa_bwd_kernel<D, true, false>)
+                         : (a.causal ? fa_bwd_kernel<D, false, true> : fa_bwd_kernel<D, false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (a.dq_sem) {

@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         // ------------------------------------------------------------ producer
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 1};
         uint32_t nunit = 0, nblk = 0;  // units / blocks issued so far
+        uint32_t nkv = 0, nq = 0, ndo = 0;  // K/V, Q and dO copies issued (for the unwinding)
         bool ok = true;
         const float inv_scale = 1.f / args.scale;
         for (int it = 0; ok; ++it) {
@@ -406,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok) ++nkv;
             ++nunit;
             for (int i_ = i0; i_ < nb && ok; ++i_, ++nblk) {
                 const int i = kDet ? block_at(un.j, i_ - i0, i0, nb, rotate) : i_;
@@ -431,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         tma_load_4d(smem + Cfg::kOffQ + st * Cfg::kTile + c * kBox, &args.tm_q,
                                     &q_full[st], 64 * c, h, sp.trow0 + i * kBlk, sp.tb);
                 }
+                ++nq;
                 uint8_t *lb = smem + Cfg::kOffLb + st * Cfg::kBias;
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
@@ -450,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                         tma_load_4d(smem + Cfg::kOffDO + c * kBox, &args.tm_do, do_full,
                                     64 * c, h, sp.trow0 + i * kBlk, sp.tb);
                 }
+                ++ndo;
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     *reinterpret_cast<uint4 *>(smem + Cfg::kOffDb + bias_off(r * 32 + lane, 0)) =
@@ -461,12 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             }
         }
         if (!ok && lane == 0) {
-            // let issued copies land before the CTA exits
-            if (nunit > 0) mbar_wait_drain(kv_full, (nunit - 1) & 1);
-            if (nblk > 0) {
-                mbar_wait_drain(&q_full[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1);
-                mbar_wait_drain(do_full, (nblk - 1) & 1);
-            }
+            // let issued copies land before the CTA exits: the last K/V pair,
+            // the last Q copy of each stage (the loop may stop between a
+            // block's Q and its dO) and the last dO
+            if (nkv > 0) mbar_wait_drain(kv_full, (nkv - 1) & 1);
+            for (uint32_t m = nq > 2 ? nq - 2 : 0; m < nq; ++m)
+                mbar_wait_drain(&q_full[m & 1], (m >> 1) & 1);
+            if (ndo > 0) mbar_wait_drain(do_full, (ndo - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer

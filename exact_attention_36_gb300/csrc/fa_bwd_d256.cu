@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x51};
         const float log2e = 1.4426950408889634f;
         uint32_t nunit = 0, n = 0;
+        uint32_t nkv = 0, nq = 0, ndo = 0;  // copies issued (for the unwinding)
         bool ok = true;
         for (int it = 0; ok; ++it) {
             Unit256 un;
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok) ++nkv;
             ++nunit;
             for (int i = first_qblock(un.j); i < nQ && ok; ++i, ++n) {
                 w.code = kErrBwdWait + 0x52;
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                         tma_load_4d(smem + Cfg::kOffQ + c * kBoxQ, &args.tm_q, q_full, 64 * c, h,
                                     sp.trow0 + i * kQB, sp.tb);
                 }
+                ++nq;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int qr = r * 32 + lane;
@@ -195,14 +198,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (ok) ++ndo;
             }
         }
         if (!ok && lane == 0) {
-            if (nunit > 0) mbar_wait_drain(kv_full, (nunit - 1) & 1);
-            if (n > 0) {
-                mbar_wait_drain(q_full, (n - 1) & 1);
-                mbar_wait_drain(do_full, (n - 1) & 1);
-            }
+            // let issued copies land before the CTA exits (only those issued:
+            // the loop may stop between a block's Q and its dO)
+            if (nkv > 0) mbar_wait_drain(kv_full, (nkv - 1) & 1);
+            if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1);
+            if (ndo > 0) mbar_wait_drain(do_full, (ndo - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer

@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0xa0};
         const float inv_scale = 1.f / args.scale;
         uint32_t nunit = 0, nq = 0, ndo = 0;  // units, Q loads, dO loads issued
+        uint32_t nkv = 0;                    // K/V loads issued
         bool ok = true;
         // rank 0: Q with its LSE bias rows into stage nq & 1; rank 1: Q alone
         auto load_q = [&](int b, int h, int i) -> bool {
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok) ++nkv;
             ++nunit;
             const int i0 = first_block(un.j);
             if (rank == 0) {
@@ -398,10 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok && lane == 0) {
             // let issued copies land before the CTA exits
-            if (nunit > 0) mbar_wait_drain(&bars[kKvFull], (nunit - 1) & 1);
-            if (nq > 0) {
-                const uint32_t st = (rank == 0) ? ((nq - 1) & 1) : 0;
-                const uint32_t use = (rank == 0) ? ((nq - 1) >> 1) : (nq - 1);
+            // (only those issued; rank 0 has two Q stages, both possibly in flight)
+            if (nkv > 0) mbar_wait_drain(&bars[kKvFull], (nkv - 1) & 1);
+            const uint32_t nst = (rank == 0) ? 2u : 1u;
+            for (uint32_t m = nq > nst ? nq - nst : 0; m < nq; ++m) {
+                const uint32_t st = (rank == 0) ? (m & 1) : 0;
+                const uint32_t use = (rank == 0) ? (m >> 1) : m;
                 mbar_wait_drain(&bars[kQFull0 + st], use & 1);
             }
             if (ndo > 0) mbar_wait_drain(&bars[kDoFull], (ndo - 1) & 1);

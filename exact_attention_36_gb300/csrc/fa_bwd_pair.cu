@@ -203,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producer
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x81};
         uint32_t nunit = 0, nblk = 0;
+        // copies issued per barrier, counted by lane 0 (for the unwinding)
+        uint32_t nkv = 0, nqs = 0, ndos = 0, ndod = 0, nqd = 0;
         bool ok = true;
         const float log2e = 1.4426950408889634f;
         const int dcol = 64 * static_cast<int>(rank);  // this CTA's half of d
@@ -226,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_4d(smem + Cfg::kOffKd + c * kBox, &args.tm_k, &bars[kKvFull],
                                     dcol, h, (2 * un.p + c) * kBlk, b);
                     }
+                    ++nkv;
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 2; ++c)
                         tma_load_4d(smem + Cfg::kOffQs + c * kHalfBox, &args.tm_q64,
                                     &bars[kQsFull], 64 * c, h, qrow, b);
+                    ++nqs;
                 }
                 // the stage written here was last read by the dS phase of block
                 // nblk - 2, which finished before dK(nblk - 2): the producer
@@ -267,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 2; ++c)
                             tma_load_4d(smem + Cfg::kOffDOs + c * kHalfBox, &args.tm_do64,
                                         &bars[kDosFull], 64 * c, h, qrow, b);
+                        ++ndos;
                     }
                     // dO columns for dV
                     w.code = kErrBwdWait + 0x84;
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&bars[kDodFull], kBox);
                         tma_load_4d(smem + Cfg::kOffDOd, &args.tm_do, &bars[kDodFull], dcol, h,
                                     i * kBlk, b);
+                        ++ndod;
                     }
                     // Q columns for dK
                     w.code = kErrBwdWait + 0x85;
@@ -283,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&bars[kQdFull], kBox);
                         tma_load_4d(smem + Cfg::kOffQd, &args.tm_q, &bars[kQdFull], dcol, h,
                                     i * kBlk, b);
+                        ++nqd;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -290,13 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok && lane == 0) {
             // let issued copies land before the CTA exits
-            if (nunit > 0) mbar_wait_drain(&bars[kKvFull], (nunit - 1) & 1);
-            if (nblk > 0) {
-                mbar_wait_drain(&bars[kQsFull], (nblk - 1) & 1);
-                mbar_wait_drain(&bars[kDosFull], (nblk - 1) & 1);
-                mbar_wait_drain(&bars[kDodFull], (nblk - 1) & 1);
-                mbar_wait_drain(&bars[kQdFull], (nblk - 1) & 1);
-            }
+            // (only the copies issued: the loop may stop part-way through a block)
+            if (nkv > 0) mbar_wait_drain(&bars[kKvFull], (nkv - 1) & 1);
+            if (nqs > 0) mbar_wait_drain(&bars[kQsFull], (nqs - 1) & 1);
+            if (ndos > 0) mbar_wait_drain(&bars[kDosFull], (ndos - 1) & 1);
+            if (ndod > 0) mbar_wait_drain(&bars[kDodFull], (ndod - 1) & 1);
+            if (nqd > 0) mbar_wait_drain(&bars[kQdFull], (nqd - 1) & 1);
         }
     }
     else if (warp == 1) {

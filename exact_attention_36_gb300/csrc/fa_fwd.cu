@@ -37,6 +37,14 @@
 // tcgen05.mma instructions from one thread execute in issue order, so S(j+1)
 // overwrites the P(j) it aliases only after PV(j) has read it, and the
 // commit that signals S(j+1) also covers PV(j) (so the softmax may rescale O).
+//
+// D = 256 (one query tile; O takes columns 256-511): S alternates between two
+// buffers, [0,128) and [128,256), and the MMA warp issues S(j+1) as soon as
+// K(j+1) is in, before it waits for P(j); then PV(j).  The tensor core works
+// on S(j+1) while the softmax of tile j runs.  K streams into ring slot 0
+// (warp 0; K(j+1) may load once S(j) is done) and V into slot 1 (warp 2), so
+// neither stream waits for the other's slot.  A rescale of O waits for PV(j-1),
+// which the commit of S(j+1) no longer covers.
 #include "fa_common.cuh"
 #include "sm100_ptx.cuh"
 #include "exp2_poly.cuh"
@@ -74,8 +82,8 @@ struct FwdCfg {
     static constexpr int kStageOff = kRingOff + kStages * kTileBytes;
     static constexpr int kBarOff = kStageOff + kStageBufs * kTileBytes;
     // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain,
-    // stage_free[2], staged[2]
-    static constexpr int kNumBars = 2 + 2 * kStages + 11;
+    // stage_free[2], staged[2], pv_done
+    static constexpr int kNumBars = 2 + 2 * kStages + 12;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -153,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint64_t *drain = s_full + 6;
     uint64_t *stage_free = s_full + 7;  // [2]: a staging buffer's TMA store has read it
     uint64_t *staged = s_full + 9;      // [2]: the four warps of a tile wrote its O rows
+    uint64_t *pv_done = s_full + 11;    // D = 256: a PV MMA completed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
 
@@ -180,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_init(&stage_free[t], 1);
             mbar_init(&staged[t], 4);
         }
+        mbar_init(pv_done, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -256,6 +266,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         }
                         ++ring;
                     }
+                } else if constexpr (Cfg::kNQ == 1) {
+                    // K_j into slot 0 (V_j streams into slot 1 from warp 2)
+                    for (int j = 0; j < n1 && ok; ++j) {
+                        w.code = kErrFwdWait + 2;
+                        if (!mbar_wait(&kv_empty[0], (ring & 1) ^ 1, w)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&kv_full[0], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_load_4d(smem + Cfg::kRingOff + c * kBox, &args.tm_k, &kv_full[0], 64 * c, h,
+                                        sp.trow0 + j * kBlockN, sp.tb);
+                        ++ring;
+                    }
                 } else {
                     for (int j = 0; j < n1 && ok; ++j) {
                         for (int which = 0; which < 2; ++which) {
@@ -278,11 +302,46 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
-                constexpr uint32_t kBufs = Cfg::kGrouped ? Cfg::kGroups : Cfg::kStages;
-                const uint32_t lo = ring > kBufs ? ring - kBufs : 0;
-                for (uint32_t r = lo; r < ring; ++r)
-                    mbar_wait_drain(&kv_full[r % kBufs], (r / kBufs) & 1);
+                if constexpr (Cfg::kNQ == 1) {
+                    if (ring > 0) mbar_wait_drain(&kv_full[0], (ring - 1) & 1);
+                } else {
+                    constexpr uint32_t kBufs = Cfg::kGrouped ? Cfg::kGroups : Cfg::kStages;
+                    const uint32_t lo = ring > kBufs ? ring - kBufs : 0;
+                    for (uint32_t r = lo; r < ring; ++r)
+                        mbar_wait_drain(&kv_full[r % kBufs], (r / kBufs) & 1);
+                }
                 if (qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ V producer (D = 256)
+        if constexpr (Cfg::kNQ == 1) {
+            if (lane == 0) {
+                WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 5};
+                uint32_t vc = 0;  // V tiles issued
+                bool ok = true;
+                for (int it = 0; ok; ++it) {
+                    Unit un;
+                    if (!unit_at(it, U, BH, P, un)) break;
+                    if (un.p < 0) continue;
+                    const int h = un.bh % H;
+                    const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
+                    if (un.p * Cfg::kRows >= sp.len) continue;
+                    int n0, n1;
+                    tiles_for(un.p, sp.len, n0, n1);
+                    for (int j = 0; j < n1 && ok; ++j) {
+                        if (!mbar_wait(&kv_empty[1], (vc & 1) ^ 1, w)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&kv_full[1], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_load_4d(smem + Cfg::kRingOff + Cfg::kTileBytes + c * kBox, &args.tm_v,
+                                        &kv_full[1], 64 * c, h, sp.trow0 + j * kBlockN, sp.tb);
+                        ++vc;
+                    }
+                }
+                if (!ok && vc > 0) mbar_wait_drain(&kv_full[1], (vc - 1) & 1);
             }
         }
     } else if (warp == 1) {
@@ -291,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 10};
             uint32_t ring = 0, qi = 0;
             uint32_t pph0 = 0, pph1 = 0;
+            uint32_t g = 0, kc = 0, vc = 0;  // D = 256: tiles, K and V tiles consumed
             const uint32_t tS0 = tmem, tS1 = tmem + 128;
             const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
             const uint32_t q0 = smem_base, q1 = smem_base + Cfg::kTileBytes;
@@ -363,6 +423,42 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                             mma_commit(&o_full[1]);
                         }
                     }
+                } else if constexpr (Cfg::kNQ == 1) {
+                    // S(j+1) into the other S buffer as soon as K(j+1) is in,
+                    // then [wait V(j), P(j)] PV(j).  Buffer and phase of tile
+                    // g (counted over the CTA's units): g & 1, (g >> 1) & 1.
+                    const uint32_t ring_v = ring_base + Cfg::kTileBytes;
+                    w.code = kErrFwdWait + 11;
+                    if (!mbar_wait(&kv_full[0], kc & 1, w)) { ok = false; break; }
+                    ++kc;
+                    tc_fence_after();
+                    issue_qk<D>(tmem + (g & 1) * 128, q0, ring_base);
+                    mma_commit(&s_full[g & 1]);
+                    mma_commit(&kv_empty[0]);
+                    if (n0 == 1) mma_commit(q_empty);
+                    for (int j = 0; j < n0; ++j, ++g) {
+                        if (j + 1 < n0) {
+                            const uint32_t bn = (g + 1) & 1;
+                            w.code = kErrFwdWait + 14;
+                            if (!mbar_wait(&kv_full[0], kc & 1, w)) { ok = false; break; }
+                            ++kc;
+                            tc_fence_after();
+                            issue_qk<D>(tmem + bn * 128, q0, ring_base);
+                            mma_commit(&s_full[bn]);
+                            mma_commit(&kv_empty[0]);
+                            if (j + 2 == n0) mma_commit(q_empty);  // the last S MMA
+                        }
+                        w.code = kErrFwdWait + 12;
+                        if (!mbar_wait(&kv_full[1], vc & 1, w)) { ok = false; break; }
+                        ++vc;
+                        w.code = kErrFwdWait + 13;
+                        if (!mbar_wait(&p_full[g & 1], (g >> 1) & 1, w)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv<D>(tO0, tmem + (g & 1) * 128, ring_v, j > 0);
+                        mma_commit(&kv_empty[1]);
+                        mma_commit(pv_done);
+                        if (j + 1 == n0) mma_commit(&o_full[0]);
+                    }
                 } else {
                     // K_j and V_j in single slots, each with its own barriers
                     const uint32_t kslot = ring % Cfg::kStages;
@@ -372,10 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     tc_fence_after();
                     issue_qk<D>(tS0, q0, ring_base + kslot * Cfg::kTileBytes);
                     mma_commit(&s_full[0]);
-                    if constexpr (Cfg::kNQ == 2) {
-                        issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
-                        mma_commit(&s_full[1]);
-                    }
+                    issue_qk<D>(tS1, q1, ring_base + kslot * Cfg::kTileBytes);
+                    mma_commit(&s_full[1]);
                     mma_commit(&kv_empty[kslot]);
                     // Q is read only by the S MMAs (see the grouped path)
                     if (n1 == 1) mma_commit(q_empty);
@@ -400,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                             pph0 ^= 1;
                             tc_fence_after();
                             issue_pv<D>(tO0, tS0, vaddr, j > 0);
-                            if constexpr (Cfg::kNQ == 1) mma_commit(&kv_empty[vslot]);
                             if (j + 1 < n0) {
                                 w.code = kErrFwdWait + 14;
                                 if (!mbar_wait(&kv_full[nslot], nphase, w)) { ok = false; break; }
@@ -408,15 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                                 tc_fence_after();
                                 issue_qk<D>(tS0, q0, naddr);
                                 mma_commit(&s_full[0]);
-                                if constexpr (Cfg::kNQ == 1) {
-                                    mma_commit(&kv_empty[nslot]);
-                                    if (j + 2 == n0) mma_commit(q_empty);  // the last S MMA
-                                }
                             } else {
                                 mma_commit(&o_full[0]);
                             }
                         }
-                        if constexpr (Cfg::kNQ == 1) continue;
                         w.code = kErrFwdWait + 15;
                         if (!mbar_wait(&p_full[1], pph1, w)) { ok = false; break; }
                         pph1 ^= 1;
@@ -449,12 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const int quarter = warp & 3;   // TMEM lane quarter this warp may access
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + t * 128 + lane_off;
         const uint32_t tO = tmem + 256 + t * D + lane_off;
         const float c2 = args.scale_log2;
         const float tau = args.rescale_threshold;
         WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 20 + t};
         uint32_t sph = 0, oph = 0;
+        uint32_t g = 0;  // D = 256: tiles processed; tile g uses S buffer g & 1
         bool ok = (t < Cfg::kNQ);
         // With grouped K/V slots one thread of tile 1 frees each group: S1(j)
         // complete means the MMAs of key tile j-1 (PV0, S0(j), PV1) are done
@@ -476,8 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             const int row = un.p * Cfg::kRows + t * kBlockM + r_in_tile;
             float m_used = -INFINITY;  // reference maximum, log2 units of scaled scores
             float l = 0.f;             // running row sum relative to m_used
-            for (int j = 0; j < n; ++j) {
-                if (!mbar_wait(&s_full[t], sph, w)) { ok = false; break; }
+            for (int j = 0; j < n; ++j, ++g) {
+                // this tile's S buffer and the phase of its barriers
+                const int buf = (Cfg::kNQ == 1) ? static_cast<int>(g & 1) : t;
+                const uint32_t spar = (Cfg::kNQ == 1) ? ((g >> 1) & 1) : sph;
+                const uint32_t tS = tmem + buf * 128 + lane_off;
+                if (!mbar_wait(&s_full[buf], spar, w)) { ok = false; break; }
                 if (releaser) mbar_arrive(&kv_empty[grp++ % Cfg::kGroups]);
                 sph ^= 1;
                 tc_fence_after();
@@ -513,6 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     const float alpha = ex2_mufu(m_used - m_new);
                     l *= alpha;
                     if (j > 0) {
+                        if constexpr (Cfg::kNQ == 1) {
+                            // S(j) was issued before PV(j-1): wait for that PV
+                            if (!mbar_wait(pv_done, (g - 1) & 1, w)) { ok = false; break; }
+                            tc_fence_after();
+                        }
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t orr[32];
@@ -567,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 l += ls.x + ls.y;
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&p_full[t]);
+                mbar_arrive(&p_full[buf]);
             }
             if (!ok) break;
             // ---- epilogue: O / l -> bf16, LSE

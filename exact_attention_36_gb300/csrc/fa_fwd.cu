@@ -41,10 +41,12 @@
 // D = 256 (one query tile; O takes columns 256-511): S alternates between two
 // buffers, [0,128) and [128,256), and the MMA warp issues S(j+1) as soon as
 // K(j+1) is in, before it waits for P(j); then PV(j).  The tensor core works
-// on S(j+1) while the softmax of tile j runs.  K streams into ring slot 0
-// (warp 0; K(j+1) may load once S(j) is done) and V into slot 1 (warp 2), so
-// neither stream waits for the other's slot.  A rescale of O waits for PV(j-1),
-// which the commit of S(j+1) no longer covers.
+// on S(j+1) while the softmax of tile j runs.  K streams in head-dim halves
+// through three 32 KB half-slots (warp 0) and V through one 64 KB slot (warp
+// 2), so neither stream waits for the other's slot, and K(j+1)'s first half
+// loads while S(j) still reads K(j); both streams are also prefetched into
+// L2 two tiles ahead.  A rescale of O waits for PV(j-1), which the commit of
+// S(j+1) no longer covers.
 #include "fa_common.cuh"
 #include "sm100_ptx.cuh"
 #include "exp2_poly.cuh"
@@ -74,16 +76,22 @@ struct FwdCfg {
     static constexpr int kGroups = kStages / 2;
     static constexpr int kQBytes = kNQ * kTileBytes;
     static constexpr int kRingOff = kQBytes;
+    // D = 256: V in one 64 KB slot at kRingOff, K in three 32 KB half-slots
+    // after it, each holding half of a K tile's head dim (S's K steps 0-7 read
+    // the first half, 8-15 the second), so K(j+1)'s first half can load while
+    // S(j) still reads K(j).  Other head dims: kStages whole-tile slots.
+    static constexpr int kKhOff = kRingOff + kTileBytes;
+    static constexpr int kRingBytes = (D == 256) ? kTileBytes + 3 * (kTileBytes / 2) : kStages * kTileBytes;
     // Epilogue staging: O of a finished tile is written here (bf16, in the
     // TMA box layout) and stored by TMA.  D = 64: one buffer per query tile;
     // D = 128: one buffer the two tiles take in turn (shared memory has room
     // for one beside Q and the ring); D = 256: none (direct stores).
     static constexpr int kStageBufs = (D == 64) ? 2 : (D == 128 ? 1 : 0);
-    static constexpr int kStageOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kStageOff = kRingOff + kRingBytes;
     static constexpr int kBarOff = kStageOff + kStageBufs * kTileBytes;
     // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain,
-    // stage_free[2], staged[2], pv_done
-    static constexpr int kNumBars = 2 + 2 * kStages + 12;
+    // stage_free[2], staged[2], pv_done, kh_full[3], kh_empty[3]
+    static constexpr int kNumBars = 2 + 2 * kStages + 18;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -132,6 +140,18 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_saddr, uint32_t
     }
 }
 
+// Half of S = Q K^T at D = 256: K steps [8 half, 8 half + 8), i.e. head-dim
+// columns [128 half, 128 half + 128), with that half of K in its own 32 KB
+// half-slot (two TMA boxes).
+__device__ __forceinline__ void issue_qk_half(uint32_t tS, uint32_t q_saddr, uint32_t kh_saddr, int half) {
+    const uint64_t qd = sdesc_sw128(q_saddr + half * 2 * kBox, 16, 1024), kd = sdesc_sw128(kh_saddr, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off16 = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+        mma_ss(tS, qd + off16, kd + off16, FwdCfg<256>::kIdescS, (half > 0 || kk > 0) ? 1u : 0u);
+    }
+}
+
 // O (+)= P V: P from TMEM, V MN-major (head dim contiguous, keys along K).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_saddr, bool acc) {
@@ -162,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint64_t *stage_free = s_full + 7;  // [2]: a staging buffer's TMA store has read it
     uint64_t *staged = s_full + 9;      // [2]: the four warps of a tile wrote its O rows
     uint64_t *pv_done = s_full + 11;    // D = 256: a PV MMA completed
+    uint64_t *kh_full = s_full + 12;    // D = 256: [3] K half-slots
+    uint64_t *kh_empty = s_full + 15;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
 
@@ -190,6 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_init(&staged[t], 4);
         }
         mbar_init(pv_done, 1);
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&kh_full[i], 1);
+            mbar_init(&kh_empty[i], 1);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -267,18 +293,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         ++ring;
                     }
                 } else if constexpr (Cfg::kNQ == 1) {
-                    // K_j into slot 0 (V_j streams into slot 1 from warp 2)
+                    // K_j in two head-dim halves through three half-slots (V_j
+                    // streams into its own slot from warp 2); half r of the
+                    // CTA's stream goes to half-slot r % 3
                     for (int j = 0; j < n1 && ok; ++j) {
-                        w.code = kErrFwdWait + 2;
-                        if (!mbar_wait(&kv_empty[0], (ring & 1) ^ 1, w)) {
-                            ok = false;
-                            break;
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t hs = ring % 3;
+                            w.code = kErrFwdWait + 2;
+                            if (!mbar_wait(&kh_empty[hs], ((ring / 3) & 1) ^ 1, w)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&kh_full[hs], Cfg::kTileBytes / 2);
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_4d(smem + Cfg::kKhOff + hs * (Cfg::kTileBytes / 2) + c * kBox, &args.tm_k,
+                                            &kh_full[hs], 64 * (2 * half + c), h, sp.trow0 + j * kBlockN, sp.tb);
+                            ++ring;
                         }
-                        mbar_arrive_expect_tx(&kv_full[0], Cfg::kTileBytes);
-                        for (int c = 0; c < Cfg::kBoxes; ++c)
-                            tma_load_4d(smem + Cfg::kRingOff + c * kBox, &args.tm_k, &kv_full[0], 64 * c, h,
-                                        sp.trow0 + j * kBlockN, sp.tb);
-                        ++ring;
+                        // a half-slot turns over only when its MMAs are done, so
+                        // a load pays its full latency: bring K(j+2) into L2
+                        if (ok && j + 2 < n1)
+                            for (int c = 0; c < Cfg::kBoxes; ++c)
+                                tma_prefetch_l2_4d(&args.tm_k, 64 * c, h, sp.trow0 + (j + 2) * kBlockN, sp.tb);
                     }
                 } else {
                     for (int j = 0; j < n1 && ok; ++j) {
@@ -303,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             if (!ok) {
                 // let the copies already issued land before the CTA exits
                 if constexpr (Cfg::kNQ == 1) {
-                    if (ring > 0) mbar_wait_drain(&kv_full[0], (ring - 1) & 1);
+                    for (uint32_t r = ring > 3 ? ring - 3 : 0; r < ring; ++r)
+                        mbar_wait_drain(&kh_full[r % 3], (r / 3) & 1);
                 } else {
                     constexpr uint32_t kBufs = Cfg::kGrouped ? Cfg::kGroups : Cfg::kStages;
                     const uint32_t lo = ring > kBufs ? ring - kBufs : 0;
@@ -336,8 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         }
                         mbar_arrive_expect_tx(&kv_full[1], Cfg::kTileBytes);
                         for (int c = 0; c < Cfg::kBoxes; ++c)
-                            tma_load_4d(smem + Cfg::kRingOff + Cfg::kTileBytes + c * kBox, &args.tm_v,
+                            tma_load_4d(smem + Cfg::kRingOff + c * kBox, &args.tm_v,
                                         &kv_full[1], 64 * c, h, sp.trow0 + j * kBlockN, sp.tb);
+                        if (j + 2 < n1)  // V(j+2) into L2 (as for K)
+                            for (int c = 0; c < Cfg::kBoxes; ++c)
+                                tma_prefetch_l2_4d(&args.tm_v, 64 * c, h, sp.trow0 + (j + 2) * kBlockN, sp.tb);
                         ++vc;
                     }
                 }
@@ -427,25 +467,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     // S(j+1) into the other S buffer as soon as K(j+1) is in,
                     // then [wait V(j), P(j)] PV(j).  Buffer and phase of tile
                     // g (counted over the CTA's units): g & 1, (g >> 1) & 1.
-                    const uint32_t ring_v = ring_base + Cfg::kTileBytes;
-                    w.code = kErrFwdWait + 11;
-                    if (!mbar_wait(&kv_full[0], kc & 1, w)) { ok = false; break; }
-                    ++kc;
-                    tc_fence_after();
-                    issue_qk<D>(tmem + (g & 1) * 128, q0, ring_base);
-                    mma_commit(&s_full[g & 1]);
-                    mma_commit(&kv_empty[0]);
+                    const uint32_t ring_v = ring_base;
+                    const uint32_t kh_base = smem_base + Cfg::kKhOff;
+                    // S of tile buffer b: two halves of K steps, each behind
+                    // its own half-slot's barrier, each half-slot released by
+                    // the commit after its eight MMAs
+                    auto issue_s = [&](uint32_t b) -> bool {
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t hs = kc % 3;
+                            w.code = kErrFwdWait + 14;
+                            if (!mbar_wait(&kh_full[hs], (kc / 3) & 1, w)) return false;
+                            ++kc;
+                            tc_fence_after();
+                            issue_qk_half(tmem + b * 128, q0, kh_base + hs * (Cfg::kTileBytes / 2), half);
+                            mma_commit(&kh_empty[hs]);
+                        }
+                        mma_commit(&s_full[b]);
+                        return true;
+                    };
+                    if (!issue_s(g & 1)) { ok = false; break; }
                     if (n0 == 1) mma_commit(q_empty);
                     for (int j = 0; j < n0; ++j, ++g) {
                         if (j + 1 < n0) {
-                            const uint32_t bn = (g + 1) & 1;
-                            w.code = kErrFwdWait + 14;
-                            if (!mbar_wait(&kv_full[0], kc & 1, w)) { ok = false; break; }
-                            ++kc;
-                            tc_fence_after();
-                            issue_qk<D>(tmem + bn * 128, q0, ring_base);
-                            mma_commit(&s_full[bn]);
-                            mma_commit(&kv_empty[0]);
+                            if (!issue_s((g + 1) & 1)) { ok = false; break; }
                             if (j + 2 == n0) mma_commit(q_empty);  // the last S MMA
                         }
                         w.code = kErrFwdWait + 12;

@@ -168,6 +168,16 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// Prefetch a 4-D tile into L2 (no shared memory, no barrier): a later
+// tma_load_4d of the same box then reads from L2.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                   int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // 3-D tiled reduce-add shared -> global (element type from the tensor map),
 // tracked by this thread's bulk async-groups.  Rows outside the tensor are
 // skipped.

@@ -320,26 +320,28 @@ def time_device(buf, causal, scale, steps, warmup, dist_on):
 def time_e2e(q, k, v, dout, buf, causal, scale, steps, warmup, dist_on):
     """The same step through the C ABI with host buffers.  Every step copies
     its Q, K, V, dO from pinned host memory and reads its dQ, dK, dV back;
-    the copies run on a second stream, double-buffered, so step k+1's inputs
-    arrive while step k computes.  Returns (ms per step, H2D bytes, D2H bytes,
-    (wall t0, wall t1) of the timed region)."""
+    the copies are double-buffered, so step k+1's inputs arrive while step k
+    computes, and uploads and read-backs run on two streams of their own (the
+    host link carries both directions at once).  Returns (ms per step, H2D
+    bytes, D2H bytes, (wall t0, wall t1) of the timed region)."""
     dev = buf.q.device
     hin = [t.pin_memory() for t in (q, k, v, dout)]
     hout = [[torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
             for _ in range(2)]
     bufs = [buf, Buffers(q, k, v, dout, dev)]
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device=dev)
+    copy_in = torch.cuda.Stream(device=dev)
+    copy_out = torch.cuda.Stream(device=dev)
     ready = [torch.cuda.Event() for _ in range(2)]  # inputs of buffer b copied
     done = [torch.cuda.Event() for _ in range(2)]   # step on buffer b computed
     fetched = [torch.cuda.Event() for _ in range(2)]  # outputs of buffer b read back
 
     def upload(b):
-        with torch.cuda.stream(copy):
-            copy.wait_event(done[b])  # the previous step on this buffer finished with it
+        with torch.cuda.stream(copy_in):
+            copy_in.wait_event(done[b])  # the previous step on this buffer finished with it
             for d, h in zip((bufs[b].q, bufs[b].k, bufs[b].v, bufs[b].dout), hin):
                 d.copy_(h, non_blocking=True)
-            ready[b].record(copy)
+            ready[b].record(copy_in)
 
     def run(nsteps):
         for b in range(2):
@@ -354,12 +356,13 @@ def time_e2e(q, k, v, dout, buf, causal, scale, steps, warmup, dist_on):
             comp.wait_event(fetched[b])  # its previous outputs were read back
             run_step(bufs[b], causal, scale)
             done[b].record(comp)
-            with torch.cuda.stream(copy):
-                copy.wait_event(done[b])
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(done[b])
                 for h, d in zip(hout[b], (bufs[b].dq, bufs[b].dk, bufs[b].dv)):
                     h.copy_(d, non_blocking=True)
-                fetched[b].record(copy)
-        comp.wait_stream(copy)
+                fetched[b].record(copy_out)
+        comp.wait_stream(copy_in)
+        comp.wait_stream(copy_out)
 
     run(warmup)
     barrier(dist_on)

@@ -41,12 +41,11 @@
 // D = 256 (one query tile; O takes columns 256-511): S alternates between two
 // buffers, [0,128) and [128,256), and the MMA warp issues S(j+1) as soon as
 // K(j+1) is in, before it waits for P(j); then PV(j).  The tensor core works
-// on S(j+1) while the softmax of tile j runs.  K streams in head-dim halves
-// through three 32 KB half-slots (warp 0) and V through one 64 KB slot (warp
-// 2), so neither stream waits for the other's slot, and K(j+1)'s first half
-// loads while S(j) still reads K(j); both streams are also prefetched into
-// L2 two tiles ahead.  A rescale of O waits for PV(j-1), which the commit of
-// S(j+1) no longer covers.
+// on S(j+1) while the softmax of tile j runs.  K (in head-dim halves) and V
+// (in key halves) stream through one ring of five 32 KB half-slots in the
+// order the MMAs read them, S(j+1)'s two halves then PV(j)'s two halves, so
+// every load can start about a key tile before it is read.  A rescale of O
+// waits for PV(j-1), which the commit of S(j+1) no longer covers.
 #include "fa_common.cuh"
 #include "sm100_ptx.cuh"
 #include "exp2_poly.cuh"
@@ -76,12 +75,12 @@ struct FwdCfg {
     static constexpr int kGroups = kStages / 2;
     static constexpr int kQBytes = kNQ * kTileBytes;
     static constexpr int kRingOff = kQBytes;
-    // D = 256: V in one 64 KB slot at kRingOff, K in three 32 KB half-slots
-    // after it, each holding half of a K tile's head dim (S's K steps 0-7 read
-    // the first half, 8-15 the second), so K(j+1)'s first half can load while
-    // S(j) still reads K(j).  Other head dims: kStages whole-tile slots.
-    static constexpr int kKhOff = kRingOff + kTileBytes;
-    static constexpr int kRingBytes = (D == 256) ? kTileBytes + 3 * (kTileBytes / 2) : kStages * kTileBytes;
+    // D = 256: five 32 KB half-slots at kRingOff, each holding half of a K
+    // tile's head dim (S's K steps 0-7 read the first half, 8-15 the second)
+    // or half of a V tile's keys (PV's K steps 0-3 / 4-7).  Other head dims:
+    // kStages whole-tile slots.
+    static constexpr int kHalfSlots = 5;
+    static constexpr int kRingBytes = (D == 256) ? kHalfSlots * (kTileBytes / 2) : kStages * kTileBytes;
     // Epilogue staging: O of a finished tile is written here (bf16, in the
     // TMA box layout) and stored by TMA.  D = 64: one buffer per query tile;
     // D = 128: one buffer the two tiles take in turn (shared memory has room
@@ -90,8 +89,8 @@ struct FwdCfg {
     static constexpr int kStageOff = kRingOff + kRingBytes;
     static constexpr int kBarOff = kStageOff + kStageBufs * kTileBytes;
     // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain,
-    // stage_free[2], staged[2], pv_done, kh_full[3], kh_empty[3]
-    static constexpr int kNumBars = 2 + 2 * kStages + 18;
+    // stage_free[2], staged[2], pv_done, hs_full[5], hs_empty[5]
+    static constexpr int kNumBars = 2 + 2 * kStages + 22;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -152,6 +151,17 @@ __device__ __forceinline__ void issue_qk_half(uint32_t tS, uint32_t q_saddr, uin
     }
 }
 
+// Half of O += P V at D = 256: keys [64 half, 64 half + 64) (K steps 4 half ..
+// 4 half + 3), that half of V in a 32 KB half-slot as four 64-row boxes, one
+// per 64 head-dim columns (MN-major, 8 KB apart).
+__device__ __forceinline__ void issue_pv_half(uint32_t tO, uint32_t tP, uint32_t vh_saddr, int half, bool acc) {
+    const uint64_t vd = sdesc_sw128(vh_saddr, kBox / 2, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_ts(tO, tP + (4 * half + kk) * 8, vd + ((kk * 2048) >> 4), FwdCfg<256>::kIdescPV,
+               (acc || kk > 0) ? 1u : 0u);
+}
+
 // O (+)= P V: P from TMEM, V MN-major (head dim contiguous, keys along K).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_saddr, bool acc) {
@@ -182,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint64_t *stage_free = s_full + 7;  // [2]: a staging buffer's TMA store has read it
     uint64_t *staged = s_full + 9;      // [2]: the four warps of a tile wrote its O rows
     uint64_t *pv_done = s_full + 11;    // D = 256: a PV MMA completed
-    uint64_t *kh_full = s_full + 12;    // D = 256: [3] K half-slots
-    uint64_t *kh_empty = s_full + 15;
+    uint64_t *hs_full = s_full + 12;    // D = 256: [5] K/V half-slots
+    uint64_t *hs_empty = s_full + 17;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
 
@@ -212,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_init(&staged[t], 4);
         }
         mbar_init(pv_done, 1);
-        for (int i = 0; i < 3; ++i) {
-            mbar_init(&kh_full[i], 1);
-            mbar_init(&kh_empty[i], 1);
+        for (int i = 0; i < 5; ++i) {
+            mbar_init(&hs_full[i], 1);
+            mbar_init(&hs_empty[i], 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -227,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tma_prefetch_desc(&args.tm_q);
         tma_prefetch_desc(&args.tm_k);
         tma_prefetch_desc(&args.tm_v);
+        if constexpr (D == 256) tma_prefetch_desc(&args.tm_v64);
     }
     tc_fence_before();
     __syncthreads();
@@ -293,28 +304,34 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         ++ring;
                     }
                 } else if constexpr (Cfg::kNQ == 1) {
-                    // K_j in two head-dim halves through three half-slots (V_j
-                    // streams into its own slot from warp 2); half r of the
-                    // CTA's stream goes to half-slot r % 3
-                    for (int j = 0; j < n1 && ok; ++j) {
-                        for (int half = 0; half < 2; ++half) {
-                            const uint32_t hs = ring % 3;
-                            w.code = kErrFwdWait + 2;
-                            if (!mbar_wait(&kh_empty[hs], ((ring / 3) & 1) ^ 1, w)) {
-                                ok = false;
-                                break;
-                            }
-                            mbar_arrive_expect_tx(&kh_full[hs], Cfg::kTileBytes / 2);
+                    // K in head-dim halves and V in key halves, one ring of
+                    // half-slots, in the order the MMAs read them: K_0, then
+                    // per key tile j: K_j+1 (if any), V_j; load r goes to
+                    // half-slot r % 5
+                    constexpr uint32_t kHalf = Cfg::kTileBytes / 2;
+                    auto load_half = [&](bool is_v, int j, int half) -> bool {
+                        const uint32_t hs = ring % Cfg::kHalfSlots;
+                        w.code = kErrFwdWait + 2;
+                        if (!mbar_wait(&hs_empty[hs], ((ring / Cfg::kHalfSlots) & 1) ^ 1, w)) return false;
+                        mbar_arrive_expect_tx(&hs_full[hs], kHalf);
+                        uint8_t *dst = smem + Cfg::kRingOff + hs * kHalf;
+                        if (is_v) {
+                            for (int c = 0; c < 4; ++c)
+                                tma_load_4d(dst + c * (kBox / 2), &args.tm_v64, &hs_full[hs], 64 * c, h,
+                                            sp.trow0 + j * kBlockN + 64 * half, sp.tb);
+                        } else {
                             for (int c = 0; c < 2; ++c)
-                                tma_load_4d(smem + Cfg::kKhOff + hs * (Cfg::kTileBytes / 2) + c * kBox, &args.tm_k,
-                                            &kh_full[hs], 64 * (2 * half + c), h, sp.trow0 + j * kBlockN, sp.tb);
-                            ++ring;
+                                tma_load_4d(dst + c * kBox, &args.tm_k, &hs_full[hs], 64 * (2 * half + c), h,
+                                            sp.trow0 + j * kBlockN, sp.tb);
                         }
-                        // a half-slot turns over only when its MMAs are done, so
-                        // a load pays its full latency: bring K(j+2) into L2
-                        if (ok && j + 2 < n1)
-                            for (int c = 0; c < Cfg::kBoxes; ++c)
-                                tma_prefetch_l2_4d(&args.tm_k, 64 * c, h, sp.trow0 + (j + 2) * kBlockN, sp.tb);
+                        ++ring;
+                        return true;
+                    };
+                    ok = load_half(false, 0, 0) && load_half(false, 0, 1);
+                    for (int j = 0; j < n1 && ok; ++j) {
+                        if (j + 1 < n1) ok = load_half(false, j + 1, 0) && load_half(false, j + 1, 1);
+                        if (ok) ok = load_half(true, j, 0) && load_half(true, j, 1);
+
                     }
                 } else {
                     for (int j = 0; j < n1 && ok; ++j) {
@@ -339,8 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             if (!ok) {
                 // let the copies already issued land before the CTA exits
                 if constexpr (Cfg::kNQ == 1) {
-                    for (uint32_t r = ring > 3 ? ring - 3 : 0; r < ring; ++r)
-                        mbar_wait_drain(&kh_full[r % 3], (r / 3) & 1);
+                    constexpr uint32_t kH = Cfg::kHalfSlots;
+                    for (uint32_t r = ring > kH ? ring - kH : 0; r < ring; ++r)
+                        mbar_wait_drain(&hs_full[r % kH], (r / kH) & 1);
                 } else {
                     constexpr uint32_t kBufs = Cfg::kGrouped ? Cfg::kGroups : Cfg::kStages;
                     const uint32_t lo = ring > kBufs ? ring - kBufs : 0;
@@ -350,47 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 if (qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
             }
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ V producer (D = 256)
-        if constexpr (Cfg::kNQ == 1) {
-            if (lane == 0) {
-                WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 5};
-                uint32_t vc = 0;  // V tiles issued
-                bool ok = true;
-                for (int it = 0; ok; ++it) {
-                    Unit un;
-                    if (!unit_at(it, U, BH, P, un)) break;
-                    if (un.p < 0) continue;
-                    const int h = un.bh % H;
-                    const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
-                    if (un.p * Cfg::kRows >= sp.len) continue;
-                    int n0, n1;
-                    tiles_for(un.p, sp.len, n0, n1);
-                    for (int j = 0; j < n1 && ok; ++j) {
-                        if (!mbar_wait(&kv_empty[1], (vc & 1) ^ 1, w)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&kv_full[1], Cfg::kTileBytes);
-                        for (int c = 0; c < Cfg::kBoxes; ++c)
-                            tma_load_4d(smem + Cfg::kRingOff + c * kBox, &args.tm_v,
-                                        &kv_full[1], 64 * c, h, sp.trow0 + j * kBlockN, sp.tb);
-                        if (j + 2 < n1)  // V(j+2) into L2 (as for K)
-                            for (int c = 0; c < Cfg::kBoxes; ++c)
-                                tma_prefetch_l2_4d(&args.tm_v, 64 * c, h, sp.trow0 + (j + 2) * kBlockN, sp.tb);
-                        ++vc;
-                    }
-                }
-                if (!ok && vc > 0) mbar_wait_drain(&kv_full[1], (vc - 1) & 1);
-            }
-        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             WaitCtx w{abort_flag, args.err_word, kErrFwdWait + 10};
             uint32_t ring = 0, qi = 0;
             uint32_t pph0 = 0, pph1 = 0;
-            uint32_t g = 0, kc = 0, vc = 0;  // D = 256: tiles, K and V tiles consumed
+            uint32_t g = 0, kc = 0;  // D = 256: tiles, half-slot loads consumed
             const uint32_t tS0 = tmem, tS1 = tmem + 128;
             const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
             const uint32_t q0 = smem_base, q1 = smem_base + Cfg::kTileBytes;
@@ -467,20 +451,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                     // S(j+1) into the other S buffer as soon as K(j+1) is in,
                     // then [wait V(j), P(j)] PV(j).  Buffer and phase of tile
                     // g (counted over the CTA's units): g & 1, (g >> 1) & 1.
-                    const uint32_t ring_v = ring_base;
-                    const uint32_t kh_base = smem_base + Cfg::kKhOff;
-                    // S of tile buffer b: two halves of K steps, each behind
-                    // its own half-slot's barrier, each half-slot released by
-                    // the commit after its eight MMAs
+                    // S of tile buffer b: two halves of K steps, then PV(j):
+                    // two halves of keys, each behind its own half-slot's
+                    // barrier and released by the commit after its MMAs
+                    constexpr uint32_t kHalf = Cfg::kTileBytes / 2;
+                    auto next_half = [&](uint32_t &addr) -> bool {
+                        const uint32_t hs = kc % Cfg::kHalfSlots;
+                        w.code = kErrFwdWait + 14;
+                        if (!mbar_wait(&hs_full[hs], (kc / Cfg::kHalfSlots) & 1, w)) return false;
+                        ++kc;
+                        tc_fence_after();
+                        addr = ring_base + hs * kHalf;
+                        return true;
+                    };
+                    auto release_half = [&](uint32_t addr) {
+                        mma_commit(&hs_empty[(addr - ring_base) / kHalf]);
+                    };
                     auto issue_s = [&](uint32_t b) -> bool {
                         for (int half = 0; half < 2; ++half) {
-                            const uint32_t hs = kc % 3;
-                            w.code = kErrFwdWait + 14;
-                            if (!mbar_wait(&kh_full[hs], (kc / 3) & 1, w)) return false;
-                            ++kc;
-                            tc_fence_after();
-                            issue_qk_half(tmem + b * 128, q0, kh_base + hs * (Cfg::kTileBytes / 2), half);
-                            mma_commit(&kh_empty[hs]);
+                            uint32_t ka;
+                            if (!next_half(ka)) return false;
+                            issue_qk_half(tmem + b * 128, q0, ka, half);
+                            release_half(ka);
                         }
                         mma_commit(&s_full[b]);
                         return true;
@@ -492,14 +484,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                             if (!issue_s((g + 1) & 1)) { ok = false; break; }
                             if (j + 2 == n0) mma_commit(q_empty);  // the last S MMA
                         }
-                        w.code = kErrFwdWait + 12;
-                        if (!mbar_wait(&kv_full[1], vc & 1, w)) { ok = false; break; }
-                        ++vc;
                         w.code = kErrFwdWait + 13;
                         if (!mbar_wait(&p_full[g & 1], (g >> 1) & 1, w)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_pv<D>(tO0, tmem + (g & 1) * 128, ring_v, j > 0);
-                        mma_commit(&kv_empty[1]);
+                        for (int half = 0; half < 2 && ok; ++half) {
+                            uint32_t va;
+                            if (!next_half(va)) { ok = false; break; }
+                            issue_pv_half(tO0, tmem + (g & 1) * 128, va, half, j > 0 || half > 0);
+                            release_half(va);
+                        }
+                        if (!ok) break;
                         mma_commit(pv_done);
                         if (j + 1 == n0) mma_commit(&o_full[0]);
                     }

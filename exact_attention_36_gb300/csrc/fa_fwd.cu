@@ -103,14 +103,17 @@ struct Unit {
     int p;   // query rows [256p, 256p + 256); -1: no unit for this CTA this round
 };
 
-// Work-unit order.  Units are numbered longest-first over the whole launch (p
-// descending, which is the order of decreasing work under a causal mask) with
-// the head index fastest; CTAs take them in a serpentine round-robin, which
-// balances the triangular causal work like an LPT list schedule.  (Keeping
-// concurrent CTAs on one head instead measured 10 % slower for causal masks
-// on GB300 and no faster without.)  Returns false when the CTA has no further
-// rounds.
-__device__ __forceinline__ bool unit_at(int it, int U, int BH, int P, Unit &out) {
+// Work-unit order; CTAs take units in a serpentine round-robin.  Without a
+// mask every unit has the same work and units are numbered head by head, so
+// the CTAs running at once share a few heads' K and V in L2 (with the head
+// index fastest and more heads than CTAs, every CTA streamed its own K/V
+// from DRAM: 718 against 1135 TFLOPS at D = 256, B = 16, H = 16, S = 1024).
+// Under a causal mask units are numbered longest-first (p descending, the
+// order of decreasing work) with the head index fastest, which balances the
+// triangular work like an LPT list schedule; with many heads, within groups
+// of gs heads (gs = BH: one group).  Returns false when the CTA has no
+// further rounds.
+__device__ __forceinline__ bool unit_at(int it, int U, int BH, int P, bool head_major, int gs, Unit &out) {
     const int G = gridDim.x;
     const int base = it * G;
     if (base >= U) return false;
@@ -120,8 +123,16 @@ __device__ __forceinline__ bool unit_at(int it, int U, int BH, int P, Unit &out)
         out.p = -1;
         return true;
     }
-    out.bh = u % BH;
-    out.p = P - 1 - u / BH;
+    if (head_major) {  // without a mask every unit has the same work
+        out.bh = u / P;
+        out.p = u % P;
+    } else {
+        // longest-first within groups of gs heads (gs = BH: over all heads)
+        const int grp = u / (gs * P), r = u - grp * gs * P;
+        const int ge = min(gs, BH - grp * gs);  // heads in this (possibly last) group
+        out.bh = grp * gs + r % ge;
+        out.p = P - 1 - r / ge;
+    }
     return true;
 }
 
@@ -203,6 +214,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int BH = args.B * H;
     const int P = (S + Cfg::kRows - 1) / Cfg::kRows;  // S: the longest sequence if packed
     const int U = BH * P;
+    // causal order: longest-first over all heads, unless more heads than half
+    // the grid would run at once with their K/V above the L2 size (128 MB);
+    // then longest-first within groups of half a grid of heads (D = 256, B = 16,
+    // H = 16, S = 1024: 568 -> 670 TFLOPS)
+    const long long kv_bytes = static_cast<long long>(min(BH, static_cast<int>(gridDim.x))) * S * D * 4;
+    const int gs = (2 * BH > static_cast<int>(gridDim.x) && kv_bytes > (128ll << 20))
+                       ? max(1, static_cast<int>(gridDim.x) / 2) : BH;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -264,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             bool ok = true;
             for (int it = 0; ok; ++it) {
                 Unit un;
-                if (!unit_at(it, U, BH, P, un)) break;
+                if (!unit_at(it, U, BH, P, !args.causal, gs, un)) break;
                 if (un.p < 0) continue;
                 const int b = un.bh / H, h = un.bh % H;
                 const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
@@ -382,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             bool ok = true;
             for (int it = 0; ok; ++it) {
                 Unit un;
-                if (!unit_at(it, U, BH, P, un)) break;
+                if (!unit_at(it, U, BH, P, !args.causal, gs, un)) break;
                 if (un.p < 0) continue;
                 const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
                 if (un.p * Cfg::kRows >= sp.len) continue;
@@ -589,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         uint32_t grp = 0;
         for (int it = 0; ok; ++it) {
             Unit un;
-            if (!unit_at(it, U, BH, P, un)) break;
+            if (!unit_at(it, U, BH, P, !args.causal, gs, un)) break;
             if (un.p < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);

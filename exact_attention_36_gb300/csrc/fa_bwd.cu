@@ -107,7 +107,10 @@ struct BUnit {
 // tile 1, ...): with the serpentine rounds that is a longest-first order
 // across heads, which balances the CTAs (head by head, the busiest CTA runs
 // about 10 % more blocks than the average at S = 32768, H = 16; the
-// fixed-order mode went from 572 to 659 TFLOPS).
+// fixed-order mode went from 572 to 659 TFLOPS).  With more heads than half
+// the grid, whose Q, dO and dQ accumulators exceed L2, the atomic-order
+// kernel numbers them tile-major within groups of half a grid of heads
+// (B = 16, H = 16, S = 2048, D = 128: 541 -> 726 TFLOPS).
 __device__ __forceinline__ void unit_coords(int u, int nT, int BH, bool causal, int &bh, int &j) {
     if (causal) {
         j = u / BH;
@@ -118,7 +121,7 @@ __device__ __forceinline__ void unit_coords(int u, int nT, int BH, bool causal, 
     }
 }
 
-__device__ __forceinline__ bool bunit_at(int it, int U, int BH, bool causal, BUnit &out) {
+__device__ __forceinline__ bool bunit_at(int it, int U, int BH, bool causal, BUnit &out, int gs = 0) {
     const int G = gridDim.x;
     const int base = it * G;
     if (base >= U) return false;
@@ -128,7 +131,16 @@ __device__ __forceinline__ bool bunit_at(int it, int U, int BH, bool causal, BUn
         out.j = -1;
         return true;
     }
-    unit_coords(u, nT_of(U, BH), BH, causal, out.bh, out.j);
+    const int nT = nT_of(U, BH);
+    if (causal && gs > 0 && gs < BH) {
+        // tile-major within groups of gs heads
+        const int grp = u / (gs * nT), r = u - grp * gs * nT;
+        const int ge = min(gs, BH - grp * gs);
+        out.j = r / ge;
+        out.bh = grp * gs + r % ge;
+        return true;
+    }
+    unit_coords(u, nT, BH, causal, out.bh, out.j);
     return true;
 }
 
@@ -325,6 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     const int BH = args.B * H;
     const int nT = (S + kBlk - 1) / kBlk;  // key tiles = query blocks
     const int U = BH * nT;
+    // atomic order under a causal mask with many heads whose Q, dO and dQ
+    // accumulator exceed L2: tile-major within groups of half a grid of heads
+    // (the fixed-order schedule keeps its own numbering)
+    const long long head_bytes = static_cast<long long>(S) * D * 8;
+    const int ugs = (!kDet && 2 * BH > static_cast<int>(gridDim.x) &&
+                     static_cast<long long>(min(BH, static_cast<int>(gridDim.x))) * head_bytes > (128ll << 20))
+                        ? max(1, static_cast<int>(gridDim.x) / 2) : 0;
     const int nSem = 8 * nT;               // deterministic-mode counters per head
     const bool rotate = kDet && !args.causal;  // see block_at
 
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         const float inv_scale = 1.f / args.scale;
         for (int it = 0; ok; ++it) {
             BUnit un;
-            if (!bunit_at(it, U, BH, kTileMajor, un)) break;
+            if (!bunit_at(it, U, BH, kTileMajor, un, ugs)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);
@@ -493,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     } while (0)
             for (int it = 0; ok; ++it) {
                 BUnit un;
-                if (!bunit_at(it, U, BH, kTileMajor, un)) break;
+                if (!bunit_at(it, U, BH, kTileMajor, un, ugs)) break;
                 if (un.j < 0) continue;
                 const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
                 if (un.j * kBlk >= sp.len) continue;
@@ -590,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         const int sw = kr & 7;  // 128B swizzle phase of this row
         for (int it = 0; ok; ++it) {
             BUnit un;
-            if (!bunit_at(it, U, BH, kTileMajor, un)) break;
+            if (!bunit_at(it, U, BH, kTileMajor, un, ugs)) break;
             if (un.j < 0) continue;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, un.bh / H);
             if (un.j * kBlk >= sp.len) continue;
@@ -735,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         bool ok = true;
         for (int it = 0; ok; ++it) {
             BUnit un;
-            if (!bunit_at(it, U, BH, kTileMajor, un)) break;
+            if (!bunit_at(it, U, BH, kTileMajor, un, ugs)) break;
             if (un.j < 0) continue;
             const int b = un.bh / H, h = un.bh % H;
             const SeqSpan sp = seq_span(args.cu_seqlens, args.T, S, b);

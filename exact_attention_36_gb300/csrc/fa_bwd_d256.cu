@@ -10,7 +10,11 @@
 //     dV, and adds the same half of dQ.  S^T and dP^T (contractions over all
 //     256 columns) are recomputed by both halves.
 //   * K_j and V_j (64 KB each) stay resident; queries stream in blocks of 64
-//     rows (Q_i and dO_i 32 KB each, one stage each).
+//     rows (Q_i and dO_i 32 KB each, one stage each).  Q_i is loaded as two
+//     head-dim halves with their own barriers: dK of output half oh reads only
+//     half oh, so the other half is released when S^T is done and the next
+//     block's copy of it loads while dP, dV and dK run; S^T takes its K steps
+//     over that half first.  LSE and Delta are double-buffered by block parity.
 //   * dQ^T = K_j[:, half]^T dS^T is formed with the head dim on the TMEM
 //     lanes (M = 128), so the drain warps hold one dQ column each.
 // Tensor Memory: X = S^T / P^T (64 cols) | Y = dP^T / dS^T / dQ^T (64 cols) |
@@ -38,9 +42,9 @@ struct Cfg {
     static constexpr int kOffDO = kOffQ + 4 * kBoxQ;  // 4 boxes
     static constexpr int kOffDS = kOffDO + 4 * kBoxQ; // 128 keys x 64 queries bf16 (16 KB)
     static constexpr int kOffRed = kOffDS + 16384;    // 2 x (64 rows x 32 fp32) dQ staging
-    static constexpr int kOffStat = kOffRed + 16384;  // 64 lse2 + 64 delta
-    static constexpr int kOffBar = kOffStat + 512;
-    static constexpr int kNumBars = 15;
+    static constexpr int kOffStat = kOffRed + 16384;  // [2] x (64 lse2 + 64 delta), by block parity
+    static constexpr int kOffBar = kOffStat + 1024;
+    static constexpr int kNumBars = 19;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked)
     static constexpr uint32_t kTX = 0, kTY = 64, kTdV = 128, kTdK = 256;
@@ -83,7 +87,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint64_t *kv_full = bars + 0, *kv_empty = bars + 1;
-    uint64_t *q_full = bars + 2, *q_empty = bars + 3;
+    // Q in two head-dim halves (boxes 0-1 and 2-3), each with its own barriers:
+    // dK of output half oh reads only half oh of Q, so the other half is
+    // released as soon as S is done and the next block's copy of it loads
+    // while dP, dV and dK run
+    uint64_t *qh_full = bars + 15, *qh_empty = bars + 17;  // [2] each
+    uint64_t *st_full = bars + 2;                          // [2]: LSE/Delta of the block written
     uint64_t *do_full = bars + 4, *do_empty = bars + 5;
     uint64_t *s_full = bars + 6, *dp_full = bars + 7;
     uint64_t *p_ready = bars + 8, *ds_ready = bars + 9;
@@ -92,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
     uint64_t *drain = bars + 14;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
-    float *stat = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // lse2[64] | delta[64]
+    float *stat_base = reinterpret_cast<float *>(smem + Cfg::kOffStat);  // [2] x (lse2[64] | delta[64])
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -104,8 +113,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
-        mbar_init(q_full, 2);  // TMA + LSE/Delta written
-        mbar_init(q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qh_full[i], 1);
+            mbar_init(&qh_empty[i], 1);
+            mbar_init(&st_full[i], 1);
+        }
         mbar_init(do_full, 1);
         mbar_init(do_empty, 1);
         mbar_init(s_full, 1);
@@ -137,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
         WaitCtx w{abort_flag, args.err_word, kErrBwdWait + 0x51};
         const float log2e = 1.4426950408889634f;
         uint32_t nunit = 0, n = 0;
-        uint32_t nkv = 0, nq = 0, ndo = 0;  // copies issued (for the unwinding)
+        uint32_t nkv = 0, ndo = 0;  // copies issued (for the unwinding)
+        uint32_t nqh[2] = {0, 0};   // Q half copies issued
         bool ok = true;
         for (int it = 0; ok; ++it) {
             Unit256 un;
@@ -165,29 +178,46 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (ok) ++nkv;
             ++nunit;
+            // per block: the early Q half (not read by dK), LSE/Delta, dO, then
+            // the late Q half (read by dK of the previous block)
+            const int eh = 1 - un.oh, lh = un.oh;
             for (int i = first_qblock(un.j); i < nQ && ok; ++i, ++n) {
-                w.code = kErrBwdWait + 0x52;
-                ok = mbar_wait(q_empty, (n & 1) ^ 1, w);
-                ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
-                if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(q_full, 4 * kBoxQ);
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_4d(smem + Cfg::kOffQ + c * kBoxQ, &args.tm_q, q_full, 64 * c, h,
-                                    sp.trow0 + i * kQB, sp.tb);
-                }
-                ++nq;
+                // LSE / Delta into registers first: their latency overlaps the waits
+                float lv[2], dv[2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int qr = r * 32 + lane;
-                    const int q = i * kQB + qr;
+                    const int q = i * kQB + r * 32 + lane;
                     const size_t x = stat_index(args.cu_seqlens, args.T, S, H, b, h, sp, q);
-                    stat[qr] = q < sp.len ? args.lse[x] * log2e : INFINITY;
-                    stat[64 + qr] = q < sp.len ? args.delta[x] : 0.f;
+                    lv[r] = q < sp.len ? args.lse[x] * log2e : INFINITY;
+                    dv[r] = q < sp.len ? args.delta[x] : 0.f;
+                }
+                auto load_q_half = [&](int hs) -> bool {
+                    w.code = kErrBwdWait + 0x52;
+                    bool good = mbar_wait(&qh_empty[hs], (n & 1) ^ 1, w);
+                    good = __all_sync(0xffffffffu, good ? 1 : 0) != 0;
+                    if (!good) return false;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&qh_full[hs], 2 * kBoxQ);
+                        for (int c = 2 * hs; c < 2 * hs + 2; ++c)
+                            tma_load_4d(smem + Cfg::kOffQ + c * kBoxQ, &args.tm_q, &qh_full[hs], 64 * c, h,
+                                        sp.trow0 + i * kQB, sp.tb);
+                    }
+                    ++nqh[hs];
+                    return true;
+                };
+                if (!load_q_half(eh)) { ok = false; break; }
+                // stats buffer n & 1 was last read by the softmax of block n - 2,
+                // whose dS preceded dQ(n - 2) and so S(n - 1), whose completion
+                // (or a later one) released the early half just waited for
+                float *st = stat_base + (n & 1) * 128;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    st[r * 32 + lane] = lv[r];
+                    st[64 + r * 32 + lane] = dv[r];
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(q_full);
+                    mbar_arrive(&st_full[n & 1]);
                     w.code = kErrBwdWait + 0x53;
                     ok = mbar_wait(do_empty, (n & 1) ^ 1, w);
                     if (ok) {
@@ -198,14 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (ok) ++ndo;
+                if (!ok) break;
+                ++ndo;
+                if (!load_q_half(lh)) { ok = false; break; }
             }
         }
         if (!ok && lane == 0) {
             // let issued copies land before the CTA exits (only those issued:
             // the loop may stop between a block's Q and its dO)
             if (nkv > 0) mbar_wait_drain(kv_full, (nkv - 1) & 1);
-            if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1);
+            for (int hs = 0; hs < 2; ++hs)
+                if (nqh[hs] > 0) mbar_wait_drain(&qh_full[hs], (nqh[hs] - 1) & 1);
             if (ndo > 0) mbar_wait_drain(do_full, (ndo - 1) & 1);
         }
     } else if (warp == 1) {
@@ -234,15 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                 FA_WAIT(kv_full, nunit & 1, 0x60);
                 if (!ok) break;
                 const int i0 = first_qblock(un.j);
+                const int eh = 1 - un.oh, lh = un.oh;
                 for (int i = i0; i < nQ; ++i, ++n) {
-                    FA_WAIT(q_full, n & 1, 0x61);
-                    if (!ok) break;
-                    tc_fence_after();
+                    // S^T over the early head-dim half first (its Q copy came in
+                    // while the previous block's dK ran), which is then released
+                    for (int g2 = 0; g2 < 2 && ok; ++g2) {
+                        const int hs = g2 ? lh : eh;
+                        FA_WAIT(&qh_full[hs], n & 1, 0x61);
+                        if (!ok) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk)
-                        mma_ss(tX, sdesc_sw128(aK + (kk / 4) * kBoxK + (kk % 4) * 32, 16, 1024),
-                               sdesc_sw128(aQ + (kk / 4) * kBoxQ + (kk % 4) * 32, 16, 1024),
-                               Cfg::kIdescSS, kk > 0 ? 1u : 0u);
+                        for (int k8 = 0; k8 < 8; ++k8) {
+                            const int kk = 8 * hs + k8;
+                            mma_ss(tX, sdesc_sw128(aK + (kk / 4) * kBoxK + (kk % 4) * 32, 16, 1024),
+                                   sdesc_sw128(aQ + (kk / 4) * kBoxQ + (kk % 4) * 32, 16, 1024),
+                                   Cfg::kIdescSS, (g2 > 0 || k8 > 0) ? 1u : 0u);
+                        }
+                        if (g2 == 0) mma_commit(&qh_empty[eh]);  // dK reads only half lh
+                    }
+                    if (!ok) break;
                     mma_commit(s_full);
                     if (n > 0) {
                         FA_WAIT(dq_empty, (n - 1) & 1, 0x62);  // the drain has read dQ(n-1)
@@ -280,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
                         mma_ts(tdK, tY + kk * 8,
                                sdesc_sw128(aQ + 2 * un.oh * kBoxQ + kk * 2048, kBoxQ, 1024),
                                Cfg::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
-                    mma_commit(q_empty);
+                    mma_commit(&qh_empty[lh]);
                     // dQ^T[half] = K_j[:, half]^T dS^T -> Y (head dim on the lanes)
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk)
@@ -321,7 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel_d256(const __grid_c
             const int key = un.j * kKeys + kr;
             for (int i = first_qblock(un.j); i < nQ; ++i, ++n) {
                 w.code = kErrBwdWait + 0x70;
-                if (!mbar_wait(q_full, n & 1, w)) { ok = false; break; }
+                if (!mbar_wait(&st_full[n & 1], (n >> 1) & 1, w)) { ok = false; break; }
+                const float *stat = stat_base + (n & 1) * 128;
                 w.code = kErrBwdWait + 0x71;
                 if (!mbar_wait(s_full, n & 1, w)) { ok = false; break; }
                 tc_fence_after();

@@ -397,6 +397,10 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     if ((st = make_map_bshd(&a.tm_v, v, mb, ms, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_do, dout, mb, ms, H, D, qrows)) != FA_OK) return st;
     if ((st = make_map_dqacc(&a.tm_dqacc, dq_acc, mb * H, ms, D, dqrows)) != FA_OK) return st;
+    if (D != 256) {
+        if ((st = make_map_bshd(&a.tm_dk32, dk, mb, ms, H, D, 32)) != FA_OK) return st;
+        if ((st = make_map_bshd(&a.tm_dv32, dv, mb, ms, H, D, 32)) != FA_OK) return st;
+    }
     if (pair && D == 256) {
         if ((st = make_map_dqacc(&a.tm_dqacc16, dq_acc, mb * H, ms, D, 16)) != FA_OK) return st;
     }

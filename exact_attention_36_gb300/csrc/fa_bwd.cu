@@ -829,8 +829,45 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             tc_fence_after();
             const int key = un.j * kBlk + r;
             const size_t orow = ((static_cast<size_t>(sp.tok0) + key) * H + h) * D;
+            // dK and dV leave by TMA stores from this warp's staging buffer (its 32
+            // key rows x 64 columns, the TMA box, 128B swizzle), unless the tile
+            // runs past its sequence in a packed batch (a store would write the
+            // next sequence's rows): then by direct stores
+            const bool use_tma = !args.cu_seqlens || (un.j + 1) * kBlk <= sp.len;
 #pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
+            for (int which = 0; which < 2 && use_tma; ++which) {
+                const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
+                const float mul = which ? args.scale : 1.f;
+                const CUtensorMap *map = which ? &args.tm_dk32 : &args.tm_dv32;
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tsrc + c * 64, v0);
+                    tmem_ld32(tsrc + c * 64 + 32, v1);
+                    tmem_ld_wait(v0);
+                    tmem_ld_wait(v1);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        pk[e] = pack_bf16x2(__uint_as_float(v0[2 * e]) * mul, __uint_as_float(v0[2 * e + 1]) * mul);
+                        pk[16 + e] = pack_bf16x2(__uint_as_float(v1[2 * e]) * mul, __uint_as_float(v1[2 * e + 1]) * mul);
+                    }
+                    if (lane == 0) bulk_wait_read<0>();  // the staging buffer has been read
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4 *>(stage_row + ((k ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(map, stage, 64 * c, h, sp.trow0 + un.j * kBlk + quarter * 32, sp.tb);
+                        bulk_commit();
+                    }
+                }
+            }
+#pragma unroll 1
+            for (int which = 0; which < 2 && !use_tma; ++which) {
                 const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
                 const float mul = which ? args.scale : 1.f;
                 uint16_t *out = reinterpret_cast<uint16_t *>(which ? args.dk : args.dv) + orow;

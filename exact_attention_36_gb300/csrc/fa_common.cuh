@@ -40,6 +40,7 @@ struct BwdArgs {
     CUtensorMap tm_dqacc;                 // fp32 [B*H, S, D], box 32 x 32 x 1
     CUtensorMap tm_dqacc16;               // D = 256 on CTA pairs: the same, box 32 x 16 x 1
     CUtensorMap tm_q64, tm_do64;          // CTA pairs: Q and dO with 64-row boxes
+    CUtensorMap tm_dk32, tm_dv32;         // D = 64/128: dK, dV with 32-row boxes (TMA-store epilogue)
     const void *o, *dout;                 // bf16 [B,S,H,D]
     const float *lse;                     // fp32 [B,H,S]
     float *dq_acc;                        // fp32 [B,H,S,D]

@@ -189,12 +189,23 @@ def bwd_varlen_semaphore_bytes(B: int, max_seqlen: int, total: int, H: int, D: i
 # ---------------------------------------------------------------- tensor API
 
 
+def _empty_problem(where: str, D: int) -> bool:
+    """Called for a problem with no elements (a size of 0, which the C ABI
+    rejects): the result is empty and nothing is launched.  The library must
+    still load and the head dim must still be one the kernels support."""
+    lib()
+    if D not in (64, 128, 256):
+        raise FAError(where, FA_ERR_UNSUPPORTED)
+    return True
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
             rescale_threshold: float = DEFAULT, poly_exp2_groups: int = DEFAULT,
             poly_exp2_degree: int = DEFAULT):
     """Exact attention forward.  q, k, v: CUDA bf16 [B, S, H, D].
 
-    Returns (o bf16 [B, S, H, D], lse fp32 [B, H, S]).
+    Returns (o bf16 [B, S, H, D], lse fp32 [B, H, S]); empty tensors when
+    B, S or H is 0.
     """
     _check_bshd("q", q)
     _check_bshd("k", k, q.shape)
@@ -204,6 +215,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if q.numel() == 0 and _empty_problem("fa_fwd", D):
+        return o, lse
     fwd(q, k, v, o, lse, causal, scale, stream, rescale_threshold, poly_exp2_groups,
         poly_exp2_degree)
     return o, lse
@@ -224,6 +237,8 @@ def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
         raise ValueError("lse: expected contiguous fp32 [B, H, S]")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    if q.numel() == 0 and _empty_problem("fa_bwd", D):
+        return torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     n = B * H * S
     ws = torch.empty(bwd_workspace_size(B, H, S, D), dtype=torch.uint8, device=q.device)
     acc_bytes = (n * D * 4 + 255) // 256 * 256
@@ -269,6 +284,8 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if q.numel() == 0 and _empty_problem("fa_fwd_varlen", D):
+        return o, lse
     fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, scale, stream)
     return o, lse
 
@@ -286,6 +303,8 @@ def backward_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: 
         raise ValueError("lse: expected contiguous fp32 [H, T]")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    if q.numel() == 0 and _empty_problem("fa_bwd_varlen", D):
+        return torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     n = H * T
     ws = torch.empty(int(lib().fa_bwd_varlen_workspace_size(T, H, D)), dtype=torch.uint8,
                      device=q.device)

@@ -16,6 +16,11 @@ Recipe (the one reading of "N(0,1) from seed" used everywhere):
   * packed batches (sequences of different lengths back to back): the same
     draw with B = 1 and S = the total token count, split by ``cu_seqlens``;
     a length mix comes from ``packed_lengths`` (its own generator, seeded).
+  * problems of several GiB per tensor (``make_qkvdo_device``): one
+    ``torch.Generator`` on the device, seeded with ``seed``; Q, K, V, dO in
+    that order, each ``torch.randn(B, S, H, D)`` drawn directly in bf16 on
+    the device (N(0,1) as torch's device generator rounds it).  The checks
+    copy the heads they compare to the host.
 """
 from __future__ import annotations
 
@@ -23,7 +28,8 @@ import math
 
 import torch
 
-__all__ = ["make_qkvdo", "make_packed", "packed_lengths", "default_scale", "WORKLOADS"]
+__all__ = ["make_qkvdo", "make_qkvdo_device", "make_packed", "packed_lengths", "default_scale",
+           "WORKLOADS"]
 
 
 def default_scale(D: int) -> float:
@@ -56,6 +62,16 @@ def make_qkvdo(B: int, H: int, S: int, D: int, seed: int = 0, stress: bool = Fal
     v = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
     dout = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
     return q, k, v, (dout if with_dout else None)
+
+
+def make_qkvdo_device(B: int, H: int, S: int, D: int, seed: int = 0, device="cuda"):
+    """Return device bf16 tensors (q, k, v, dout) of shape [B, S, H, D], drawn
+    on the device (for problems too large to draw on the host)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    shape = (B, S, H, D)
+    return tuple(torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device)
+                 for _ in range(4))
 
 
 # The workloads the library is measured and checked on: (name, B, H, S, D,

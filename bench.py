@@ -669,7 +669,8 @@ def main():
                      "frac_of_sustained": achieved / peak_sus if peak_sus else None,
                      "sm_mhz_during_call": mhz_n},
         "e2e": {"value": job_tflops(world, ff + fb, e2e_ms), "unit": "TFLOPS",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "sm_mhz": clk.region_mhz("e2e")},
         # fa_fwd 1 + fa_bwd 3 (4 in the fixed-order mode) per step of the value's region
         "gpu_launches": (5 if args.deterministic else 4) * args.steps,
         "clocks": clocks,

@@ -302,7 +302,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     if ((st = make_map_bshd(&a.tm_q, q, mb, ms, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_k, k, mb, ms, H, D)) != FA_OK) return st;
     if ((st = make_map_bshd(&a.tm_v, v, mb, ms, H, D)) != FA_OK) return st;
-    if ((st = make_map_bshd(&a.tm_o, o, mb, ms, H, D)) != FA_OK) return st;
+    if ((st = make_map_bshd(&a.tm_o, o, mb, ms, H, D, 32)) != FA_OK) return st;
     if (D == 256 && (st = make_map_bshd(&a.tm_v64, v, mb, ms, H, D, 64)) != FA_OK) return st;
     a.o = o;
     a.lse = lse;

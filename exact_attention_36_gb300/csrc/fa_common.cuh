@@ -19,7 +19,7 @@ enum DeviceError : int {
 
 struct FwdArgs {
     CUtensorMap tm_q, tm_k, tm_v;  // bf16 [B,S,H,D], box 64 x 1 x 128 x 1, 128B swizzle
-    CUtensorMap tm_o;              // the output, same geometry (TMA-store epilogue)
+    CUtensorMap tm_o;              // the output, box 64 x 1 x 32 x 1 (one warp's rows; TMA-store epilogue)
     CUtensorMap tm_v64;            // D = 256: V with 64-row boxes (key halves of a tile)
     void *o;                       // bf16 [B,S,H,D]
     float *lse;                    // fp32 [B,H,S]

@@ -57,6 +57,7 @@ constexpr int kThreads = 384;
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per tile
 constexpr int kBox = 16384;   // one TMA box: 128 rows x 64 bf16 (128 B), 128B swizzle
+constexpr int kWarpStage = 4096;  // one warp's O staging: 32 rows x 64 bf16, 128B swizzle
 
 template <int D>
 struct FwdCfg {
@@ -81,16 +82,15 @@ struct FwdCfg {
     // kStages whole-tile slots.
     static constexpr int kHalfSlots = 5;
     static constexpr int kRingBytes = (D == 256) ? kHalfSlots * (kTileBytes / 2) : kStages * kTileBytes;
-    // Epilogue staging: O of a finished tile is written here (bf16, in the
-    // TMA box layout) and stored by TMA.  D = 64: one buffer per query tile;
-    // D = 128: one buffer the two tiles take in turn (shared memory has room
-    // for one beside Q and the ring); D = 256: none (direct stores).
-    static constexpr int kStageBufs = (D == 64) ? 2 : (D == 128 ? 1 : 0);
+    // Epilogue staging: 4 KB per softmax warp (its 32 rows x 64 columns of O
+    // in bf16, the TMA box layout), from which O leaves by TMA stores.
+    // D = 256: none (no room beside Q and the ring; direct stores).
+    static constexpr bool kTmaEpilogue = (D != 256);
     static constexpr int kStageOff = kRingOff + kRingBytes;
-    static constexpr int kBarOff = kStageOff + kStageBufs * kTileBytes;
+    static constexpr int kBarOff = kStageOff + (kTmaEpilogue ? 8 * kWarpStage : 0);
     // q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain,
-    // stage_free[2], staged[2], pv_done, hs_full[5], hs_empty[5]
-    static constexpr int kNumBars = 2 + 2 * kStages + 22;
+    // pv_done, hs_full[5], hs_empty[5]
+    static constexpr int kNumBars = 2 + 2 * kStages + 18;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -200,11 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint64_t *p_full = s_full + 2;
     uint64_t *o_full = s_full + 4;
     uint64_t *drain = s_full + 6;
-    uint64_t *stage_free = s_full + 7;  // [2]: a staging buffer's TMA store has read it
-    uint64_t *staged = s_full + 9;      // [2]: the four warps of a tile wrote its O rows
-    uint64_t *pv_done = s_full + 11;    // D = 256: a PV MMA completed
-    uint64_t *hs_full = s_full + 12;    // D = 256: [5] K/V half-slots
-    uint64_t *hs_empty = s_full + 17;
+    uint64_t *pv_done = s_full + 7;     // D = 256: a PV MMA completed
+    uint64_t *hs_full = s_full + 8;     // D = 256: [5] K/V half-slots
+    uint64_t *hs_empty = s_full + 13;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
 
@@ -235,10 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_init(&o_full[t], 1);
         }
         mbar_init(drain, 1);
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(&stage_free[t], 1);
-            mbar_init(&staged[t], 4);
-        }
         mbar_init(pv_done, 1);
         for (int i = 0; i < 5; ++i) {
             mbar_init(&hs_full[i], 1);
@@ -731,63 +725,51 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             const int tile_row0 = un.p * Cfg::kRows + t * kBlockM;
             uint16_t *orow = reinterpret_cast<uint16_t *>(args.o) +
                              ((static_cast<size_t>(sp.tok0) + row) * H + h) * D;
-            if constexpr (Cfg::kStageBufs > 0) {
-                // O goes through a shared-memory tile in the TMA box layout and
-                // leaves in one TMA store per 64 columns (16-byte shared stores
-                // instead of 16-byte global stores 4 KB apart).  The k-th use of
-                // a buffer waits for the (k-1)-th release (parity (k & 1) ^ 1).
-                // D = 64: one buffer per tile, k = this tile's unit count, whose
-                // parity oph now holds (k + 1); D = 128: the tiles take the one
-                // buffer in turn, k = 2u + t, so the parity is t's.
-                const int buf = (Cfg::kStageBufs == 2) ? t : 0;
-                const uint32_t use_par = (Cfg::kStageBufs == 2) ? (oph ^ 1) : static_cast<uint32_t>(t);
-                // a packed batch's last tile of a sequence would overwrite the
-                // next sequence's rows: that tile keeps direct stores
-                const bool use_tma = !args.cu_seqlens || tile_row0 + kBlockM <= len;
-                if (!mbar_wait(&stage_free[buf], use_par ^ 1, w)) { ok = false; break; }
-                uint8_t *stg = smem + Cfg::kStageOff + buf * Cfg::kTileBytes;
+            if constexpr (Cfg::kTmaEpilogue) {
+                // Each warp writes its own 32 rows of O: 64 columns at a time
+                // into its 4 KB of the staging area (the TMA box layout, 128B
+                // swizzle), then one TMA store per 64 columns issued by its lane
+                // 0.  No warp waits for another, and the last store's read of
+                // shared memory is waited for only before the region is written
+                // again (the next 64 columns, or the next unit).  A warp whose
+                // rows run past a packed sequence's end would overwrite the next
+                // sequence's rows: it keeps direct stores.
+                const int wrow0 = tile_row0 + quarter * 32;  // this warp's first row
+                const bool use_tma = !args.cu_seqlens || wrow0 + 32 <= len;
+                uint8_t *stg = smem + Cfg::kStageOff + (t * 4 + quarter) * kWarpStage;
+                uint8_t *srow = stg + lane * 128;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t orr[32];
-                    tmem_ld32(tO + c * 32, orr);
-                    tmem_ld_wait(orr);
-                    uint32_t pk[16];
+                for (int hc = 0; hc < D / 64; ++hc) {
+                    uint32_t orr[2][32];
+                    tmem_ld32(tO + hc * 64, orr[0]);
+                    tmem_ld32(tO + hc * 64 + 32, orr[1]);
+                    tmem_ld_wait(orr[0]);
+                    tmem_ld_wait(orr[1]);
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                                            __uint_as_float(orr[2 * e + 1]) * inv_l);
+                    for (int e = 0; e < 32; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(orr[e >> 4][2 * (e & 15)]) * inv_l,
+                                            __uint_as_float(orr[e >> 4][2 * (e & 15) + 1]) * inv_l);
                     if (use_tma) {
-                        // row r_in_tile of box c/2: 16-byte chunks (c%2)*4 + v4,
-                        // 128B swizzle (chunk index xor row % 8)
-                        uint8_t *srow = stg + (c >> 1) * kBox + r_in_tile * 128;
+                        if (lane == 0) bulk_wait_read<0>();  // this region's last store has read it
+                        __syncwarp();
+                        // row `lane` of the box: 16-byte chunk k at (k ^ (lane % 8)) * 16
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            *reinterpret_cast<uint4 *>(
-                                srow + ((((c & 1) * 4 + v4) ^ (r_in_tile & 7)) << 4)) =
-                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                           pk[4 * v4 + 3]);
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4 *>(srow + ((k ^ (lane & 7)) << 4)) =
+                                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_4d(&args.tm_o, stg, 64 * hc, h, sp.trow0 + wrow0, sp.tb);
+                            bulk_commit();
+                        }
                     } else if (row < len) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + hc * 64);
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                                 pk[4 * v4 + 3]);
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                     }
-                }
-                if (use_tma) fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&staged[buf]);
-                if (r_in_tile == 0) {  // the tile's TMA stores of O
-                    if (!mbar_wait(&staged[buf], use_par, w)) { ok = false; break; }
-                    if (use_tma) {
-#pragma unroll
-                        for (int c = 0; c < Cfg::kBoxes; ++c)
-                            tma_store_4d(&args.tm_o, stg + c * kBox, 64 * c, h,
-                                         sp.trow0 + tile_row0, sp.tb);
-                        bulk_commit();
-                        bulk_wait_read<0>();  // the buffer has been read
-                    }
-                    mbar_arrive(&stage_free[buf]);
                 }
             } else {
 #pragma unroll 1
@@ -813,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 args.lse[stat_index(args.cu_seqlens, args.T, S, H, b, h, sp, row)] =
                     (m_used + log2f(l)) * 0.69314718055994531f;
         }
-        if (Cfg::kStageBufs > 0 && r_in_tile == 0) bulk_wait<0>();  // its O stores are complete
+        if (Cfg::kTmaEpilogue && lane == 0) bulk_wait<0>();  // its O stores are complete
     }
 
     tc_fence_before();

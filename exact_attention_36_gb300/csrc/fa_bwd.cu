@@ -80,8 +80,8 @@ struct BwdCfg {
     static constexpr int kOffDb = kOffLb + 2 * kBias;
     static constexpr int kOffBar = kOffDb + kBias;
     // kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full,
-    // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dkdv_empty, drain
-    static constexpr int kNumBars = 17;
+    // p_ready, ds_ready, dq_full, dq_empty, dkdv_full, dv_empty, drain, dk_empty
+    static constexpr int kNumBars = 18;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     // no alignment slack: the dynamic shared memory base must be 1024-byte
     // aligned (checked at kernel entry)
@@ -326,8 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
     uint64_t *s_full = bars + 8, *dp_full = bars + 9;
     uint64_t *p_ready = bars + 10, *ds_ready = bars + 11;
     uint64_t *dq_full = bars + 12, *dq_empty = bars + 13;
-    uint64_t *dkdv_full = bars + 14, *dkdv_empty = bars + 15;
-    uint64_t *drain = bars + 16;
+    // dkdv_full: a unit's dV and dK are complete; dv_empty / dk_empty: the drain
+    // warps have read the dV / dK accumulator (the next unit may overwrite it)
+    uint64_t *dkdv_full = bars + 14, *dv_empty = bars + 15;
+    uint64_t *drain = bars + 16, *dk_empty = bars + 17;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
 
@@ -363,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, 128);
         mbar_init(dkdv_full, 1);
-        mbar_init(dkdv_empty, 128);
+        mbar_init(dv_empty, 128);
+        mbar_init(dk_empty, 128);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -412,22 +415,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             if (un.j * kBlk >= sp.len) continue;  // past this sequence's end
             const int nb = (sp.len + kBlk - 1) / kBlk;
             const int i0 = first_block(un.j, args.causal);
-            if (lane == 0) {
-                w.code = kErrBwdWait + 1;
-                ok = mbar_wait(kv_empty, (nunit & 1) ^ 1, w);
-                if (ok) {
-                    mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
-                    for (int c = 0; c < Cfg::kBoxes; ++c) {
-                        tma_load_4d(smem + Cfg::kOffK + c * kBox, &args.tm_k, kv_full, 64 * c, h,
-                                    sp.trow0 + un.j * kBlk, sp.tb);
-                        tma_load_4d(smem + Cfg::kOffV + c * kBox, &args.tm_v, kv_full, 64 * c, h,
-                                    sp.trow0 + un.j * kBlk, sp.tb);
+            // K and V of this unit load after its first block's Q and dO: the
+            // previous unit frees their buffers earlier (its second-to-last dK,
+            // its last dV) than K and V (its last dK), so the first block's
+            // copies and -LSE / -Delta rows are in place when K and V arrive
+            const uint32_t kv_par = (nunit & 1) ^ 1;
+            ++nunit;
+            auto load_kv = [&]() {
+                if (lane == 0) {
+                    w.code = kErrBwdWait + 1;
+                    ok = mbar_wait(kv_empty, kv_par, w);
+                    if (ok) {
+                        mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTile);
+                        for (int c = 0; c < Cfg::kBoxes; ++c) {
+                            tma_load_4d(smem + Cfg::kOffK + c * kBox, &args.tm_k, kv_full, 64 * c, h,
+                                        sp.trow0 + un.j * kBlk, sp.tb);
+                            tma_load_4d(smem + Cfg::kOffV + c * kBox, &args.tm_v, kv_full, 64 * c, h,
+                                        sp.trow0 + un.j * kBlk, sp.tb);
+                        }
                     }
                 }
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (ok) ++nkv;
-            ++nunit;
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (ok) ++nkv;
+            };
+            // (fixed order: K and V first; the later K/V copy measured 2-3 % slower there)
+            if constexpr (kDet) load_kv();
             for (int i_ = i0; i_ < nb && ok; ++i_, ++nblk) {
                 const int i = kDet ? block_at(un.j, i_ - i0, i0, nb, rotate) : i_;
                 const int st = nblk & 1;
@@ -441,7 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     lv[r] = q < sp.len ? -args.lse[x] * inv_scale : -INFINITY;
                     dv[r] = q < sp.len ? -args.delta[x] : 0.f;
                 }
-                // Q_i into stage st, then the bias rows of S^T
+                // Q_i into stage st with the bias rows of S^T, then dO_i (single
+                // stage: the previous block's dV MMA, and so its dP^T, has
+                // finished) with the bias rows of dP^T.  A unit's first block
+                // issues both copies, then the unit's K and V, and writes its
+                // rows last: the rows wait for the -LSE / -Delta loads, which
+                // must not hold up the K/V copy
+                const bool first_blk = !kDet && i_ == i0;
                 w.code = kErrBwdWait + 2;
                 ok = mbar_wait(&q_empty[st], ((nblk >> 1) & 1) ^ 1, w);
                 ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
@@ -453,19 +471,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                                     &q_full[st], 64 * c, h, sp.trow0 + i * kBlk, sp.tb);
                 }
                 ++nq;
-                uint8_t *lb = smem + Cfg::kOffLb + st * Cfg::kBias;
+                auto q_rows = [&]() {
+                    uint8_t *lb = smem + Cfg::kOffLb + st * Cfg::kBias;
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    *reinterpret_cast<uint4 *>(lb + bias_off(r * 32 + lane, 0)) = bias_row(lv[r]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&q_full[st]);
-                // dO_i (single stage: the previous block's dV MMA, and so its
-                // dP^T, has finished), then the bias rows of dP^T
+                    for (int r = 0; r < 4; ++r)
+                        *reinterpret_cast<uint4 *>(lb + bias_off(r * 32 + lane, 0)) = bias_row(lv[r]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&q_full[st]);
+                };
+                if (!first_blk) q_rows();
                 w.code = kErrBwdWait + 3;
                 ok = mbar_wait(do_empty, (nblk & 1) ^ 1, w);
                 ok = __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
-                if (!ok) break;
+                if (!ok) {
+                    if (first_blk) q_rows();  // Q's barrier phase completes for the unwinding
+                    break;
+                }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(do_full, Cfg::kTile);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
@@ -473,6 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                                     64 * c, h, sp.trow0 + i * kBlk, sp.tb);
                 }
                 ++ndo;
+                if (first_blk) {
+                    load_kv();  // on failure the rows below still complete Q's and dO's phases
+                    q_rows();
+                }
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     *reinterpret_cast<uint4 *>(smem + Cfg::kOffDb + bias_off(r * 32 + lane, 0)) =
@@ -548,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     if (!ok) break;
                     ph_p ^= 1;
                     if (first && nunit > 0) {
-                        // previous unit's dK/dV epilogue has read the accumulators
-                        FA_WAIT(dkdv_empty, (nunit - 1) & 1, 15);
+                        // the previous unit's epilogue has read the dV accumulator
+                        FA_WAIT(dv_empty, (nunit - 1) & 1, 15);
                         if (!ok) break;
                     }
                     tc_fence_after();
@@ -572,6 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
                     // dS from shared memory, which leaves Y to dQ
                     issue_dq<D>(tY, aDS, aK);
                     mma_commit(dq_full);
+                    if (first && nunit > 0) {
+                        // the previous unit's epilogue has read the dK accumulator
+                        FA_WAIT(dk_empty, (nunit - 1) & 1, 20);
+                        if (!ok) break;
+                    }
                     issue_dk<D>(tdK, aDS, sbase + Cfg::kOffQ + st * Cfg::kTile, !first);
                     mma_commit(&q_empty[st]);
                     if (has_next) {
@@ -829,69 +860,67 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_kernel(const __grid_consta
             tc_fence_after();
             const int key = un.j * kBlk + r;
             const size_t orow = ((static_cast<size_t>(sp.tok0) + key) * H + h) * D;
-            // dK and dV leave by TMA stores from this warp's staging buffer (its 32
-            // key rows x 64 columns, the TMA box, 128B swizzle), unless the tile
-            // runs past its sequence in a packed batch (a store would write the
-            // next sequence's rows): then by direct stores
+            // dV, then dK.  Atomic order: each accumulator's columns are read
+            // into registers and packed to bf16 first, and released (dv_empty /
+            // dk_empty) before they are written out, so the next unit's first dV
+            // and dK MMAs wait only for the reads.  Fixed order: 64 columns at a
+            // time, released after the last (holding a whole accumulator costs
+            // that instance register spills).  They leave by TMA stores from this
+            // warp's staging buffer (its 32 key rows x 64 columns, the TMA box,
+            // 128B swizzle), unless the tile runs past its sequence in a packed
+            // batch (a store would write the next sequence's rows): then by
+            // direct stores.
             const bool use_tma = !args.cu_seqlens || (un.j + 1) * kBlk <= sp.len;
+            constexpr int kHeld = kDet ? 64 : D;  // columns held in registers at once
 #pragma unroll 1
-            for (int which = 0; which < 2 && use_tma; ++which) {
+            for (int which = 0; which < 2; ++which) {
                 const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
                 const float mul = which ? args.scale : 1.f;
                 const CUtensorMap *map = which ? &args.tm_dk32 : &args.tm_dv32;
-#pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tsrc + c * 64, v0);
-                    tmem_ld32(tsrc + c * 64 + 32, v1);
-                    tmem_ld_wait(v0);
-                    tmem_ld_wait(v1);
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        pk[e] = pack_bf16x2(__uint_as_float(v0[2 * e]) * mul, __uint_as_float(v0[2 * e + 1]) * mul);
-                        pk[16 + e] = pack_bf16x2(__uint_as_float(v1[2 * e]) * mul, __uint_as_float(v1[2 * e + 1]) * mul);
-                    }
-                    if (lane == 0) bulk_wait_read<0>();  // the staging buffer has been read
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<uint4 *>(stage_row + ((k ^ (lane & 7)) << 4)) =
-                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_4d(map, stage, 64 * c, h, sp.trow0 + un.j * kBlk + quarter * 32, sp.tb);
-                        bulk_commit();
-                    }
-                }
-            }
-#pragma unroll 1
-            for (int which = 0; which < 2 && !use_tma; ++which) {
-                const uint32_t tsrc = tmem + lane_off + (which ? Cfg::kTdK : Cfg::kTdV);
-                const float mul = which ? args.scale : 1.f;
                 uint16_t *out = reinterpret_cast<uint16_t *>(which ? args.dk : args.dv) + orow;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tsrc + c * 32, v);
-                    tmem_ld_wait(v);
-                    uint32_t pk[16];
+                for (int c0 = 0; c0 < D; c0 += kHeld) {
+                    uint32_t pk[kHeld / 2];  // columns c0 + 2e, c0 + 2e + 1 in pk[e]
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
-                                            __uint_as_float(v[2 * e + 1]) * mul);
-                    if (key < sp.len) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+                    for (int c = 0; c < kHeld / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tsrc + c0 + c * 32, v);
+                        tmem_ld_wait(v);
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                                 pk[4 * v4 + 3]);
+                        for (int e = 0; e < 16; ++e)
+                            pk[16 * c + e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
+                                                         __uint_as_float(v[2 * e + 1]) * mul);
+                    }
+                    if (c0 + kHeld == D) {  // the accumulator has been read
+                        tc_fence_before();
+                        mbar_arrive(which ? dk_empty : dv_empty);
+                    }
+                    if (use_tma) {
+#pragma unroll
+                        for (int c = 0; c < kHeld / 64; ++c) {
+                            if (lane == 0) bulk_wait_read<0>();  // the staging buffer has been read
+                            __syncwarp();
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                *reinterpret_cast<uint4 *>(stage_row + ((k ^ (lane & 7)) << 4)) =
+                                    make_uint4(pk[32 * c + 4 * k], pk[32 * c + 4 * k + 1],
+                                               pk[32 * c + 4 * k + 2], pk[32 * c + 4 * k + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_4d(map, stage, c0 + 64 * c, h,
+                                             sp.trow0 + un.j * kBlk + quarter * 32, sp.tb);
+                                bulk_commit();
+                            }
+                        }
+                    } else if (key < sp.len) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + c0);
+#pragma unroll
+                        for (int k = 0; k < kHeld / 8; ++k)
+                            dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(dkdv_empty);
         }
         if (lane == 0) bulk_wait<0>();  // every drain warp's reductions have read shared memory
     }

@@ -143,3 +143,12 @@ def test_exp2_polynomial_coefficients_meet_the_bound(deg):
     err = np.abs(p / oracle.exp2(f) - 1.0).max()
     assert err <= 2.0 ** -9
     assert err <= (8e-5 if deg == 3 else 2e-7)
+
+
+def test_empty_problem_rule_needs_no_device(lib):
+    # the tensor API answers a problem with a size of 0 with empty results and
+    # launches nothing, but still refuses a head dim the kernels do not have
+    for D in (64, 128, 256):
+        assert fa._empty_problem("fa_fwd", D)
+    with pytest.raises(fa.FAError):
+        fa._empty_problem("fa_fwd", 96)

@@ -1,0 +1,180 @@
+"""CPU model of the D = 128 forward kernel's pipeline protocol (no GPU).
+
+The forward runs, per CTA, a producer warp (the unit's two Q tiles, then K and
+V through a ring of four shared-memory slots used as two groups {V_j, K_j+1},
+one full and one empty barrier per group), one MMA-issuing thread and the
+softmax warps of query tiles 0 and 1 (each also writes its tile's O and LSE).
+Per key tile the MMA thread issues PV0(j), S0(j+1), PV1(j), S1(j+1); S and P
+of a tile share one TMEM region, O of each tile accumulates in its own.  A
+group is released by one thread of tile 1's softmax when it sees S1(j+1)
+complete (the group's last reader, issued after every other MMA that reads it)
+or, for the unit's last group, O1; Q is released after the unit's last S MMA.
+The softmax rescales O in TMEM when the running maximum jumps, between two PV
+MMAs.
+
+This module restates each role in the kernel's order (waits with the kernel's
+parity expressions) and runs them with random durations, unit lengths and
+causal tile counts (tile 0 one key tile short), checking that every role
+finishes, that every parity wait sees exactly its phase, and that no buffer
+(Q, the K and V slots, S/P and O in TMEM) is written while a previous use is
+still read.  Planted mistakes (a wait or a release moved) must be caught.
+"""
+import random
+
+import pytest
+
+from tests._pipeline_sim import Barrier, Sim, Violation
+
+GROUPS = 2  # slot groups {V_j, K_j+1} of the four-slot ring
+
+
+def make_bars():
+    B = Barrier
+    bars = {'q_full': B('q_full', 1), 'q_empty': B('q_empty', 1)}
+    for g in range(GROUPS):
+        bars[f'kv_full{g}'] = B(f'kv_full{g}', 1)
+        bars[f'kv_empty{g}'] = B(f'kv_empty{g}', 1)
+    for t in range(2):
+        bars[f's_full{t}'] = B(f's_full{t}', 1)
+        bars[f'p_full{t}'] = B(f'p_full{t}', 1)
+        bars[f'o_full{t}'] = B(f'o_full{t}', 1)
+    return bars
+
+
+def producer(b, units, rng, skip=()):
+    ring = 0
+    f = rng.uniform(0.1, 5.0)
+    for u, (n0, n1) in enumerate(units):
+        yield ('wait', b['q_empty'], (u & 1) ^ 1, u - 1)
+        yield ('arrive_tx', b['q_full'], 1)
+        yield ('tma', b['q_full'], 1, 'Q', u)
+        for j in range(-1, n1):
+            g, use = ring % GROUPS, ring // GROUPS
+            if 'kv_empty' not in skip:
+                yield ('wait', b[f'kv_empty{g}'], (use & 1) ^ 1, use - 1)
+            has_v, has_k = j >= 0, j + 1 < n1
+            yield ('arrive_tx', b[f'kv_full{g}'], int(has_v) + int(has_k))
+            if has_v:
+                yield ('tma', b[f'kv_full{g}'], 1, f'V{g}', use)
+            if has_k:
+                yield ('tma', b[f'kv_full{g}'], 1, f'K{g}', use)
+            yield ('delay', f * rng.uniform(0, 30))
+            ring += 1
+
+
+def mma(b, units, skip=()):
+    ring = 0
+    jj = [0, 0]  # S/P tiles seen by each query tile (TMEM S/P uses 2jj, 2jj + 1)
+    for u, (n0, n1) in enumerate(units):
+        yield ('wait', b['q_full'], u & 1, u)
+        g, use = ring % GROUPS, ring // GROUPS
+        yield ('wait', b[f'kv_full{g}'], use & 1, use)
+        ring += 1
+        kk = (f'K{g}', use)
+        yield ('mma', [('Q', u), kk], [('SP0', 2 * jj[0])])
+        yield ('commit', b['s_full0'])
+        yield ('mma', [('Q', u), kk], [('SP1', 2 * jj[1])])
+        yield ('commit', b['s_full1'])
+        if n1 == 1:
+            yield ('commit', b['q_empty'])
+        for j in range(n1):
+            g, use = ring % GROUPS, ring // GROUPS
+            yield ('wait', b[f'kv_full{g}'], use & 1, use)
+            ring += 1
+            vv, kk = (f'V{g}', use), (f'K{g}', use)
+            if j < n0:
+                if 'p_full' not in skip:
+                    yield ('wait', b['p_full0'], jj[0] & 1, jj[0])
+                yield ('mma', [('SP0', 2 * jj[0] + 1), vv], [('O0', (u, 2 * j))])
+                jj[0] += 1
+                if j + 1 < n0:
+                    yield ('mma', [('Q', u), kk], [('SP0', 2 * jj[0])])
+                    yield ('commit', b['s_full0'])
+                else:
+                    yield ('commit', b['o_full0'])
+            yield ('wait', b['p_full1'], jj[1] & 1, jj[1])
+            yield ('mma', [('SP1', 2 * jj[1] + 1), vv], [('O1', (u, 2 * j))])
+            jj[1] += 1
+            if j + 1 < n1:
+                if 'q_empty_early' in skip and j + 2 == n1:
+                    yield ('commit', b['q_empty'])  # planted: before the last S MMA
+                yield ('mma', [('Q', u), kk], [('SP1', 2 * jj[1])])
+                yield ('commit', b['s_full1'])
+                if j + 2 == n1 and 'q_empty_early' not in skip:
+                    yield ('commit', b['q_empty'])  # the last S MMA
+            else:
+                yield ('commit', b['o_full1'])
+
+
+def softmax(b, units, t, rng, skip=()):
+    f = rng.uniform(0.1, 5.0)
+    jj = 0
+    grp = 0  # groups released (tile 1)
+    for u, (n0, n1) in enumerate(units):
+        n = n1 if t else n0
+        for j in range(n):
+            yield ('wait', b[f's_full{t}'], jj & 1, jj)
+            if t == 1:
+                yield ('arrive', b[f'kv_empty{grp % GROUPS}'])
+                grp += 1
+                if 'release_early' in skip and j == 0:
+                    # planted: {V_0, K_1} released with {K_0}, before its readers ran
+                    yield ('arrive', b[f'kv_empty{grp % GROUPS}'])
+                    grp += 1
+            yield ('ld', f'SP{t}', 2 * jj)
+            if j > 0 and rng.random() < 0.3:
+                # conditional rescale of O between PV(j-1) and PV(j): reads
+                # PV(j-1)'s sum, writes the rescaled one
+                yield ('ld', f'O{t}', (u, 2 * j - 2))
+                yield ('st', f'O{t}', (u, 2 * j - 1))
+            yield ('delay', f * rng.uniform(300, 1500))
+            yield ('st', f'SP{t}', 2 * jj + 1)
+            yield ('arrive', b[f'p_full{t}'])
+            jj += 1
+        yield ('wait', b[f'o_full{t}'], u & 1, u)
+        if t == 1 and 'release_early' not in skip:
+            yield ('arrive', b[f'kv_empty{grp % GROUPS}'])  # the unit's last group
+            grp += 1
+        yield ('ld', f'O{t}', (u, 2 * (n - 1)))
+        yield ('delay', f * rng.uniform(200, 3000))  # staging, stores, LSE
+
+
+def simulate(seed, skip=()):
+    rng = random.Random(seed)
+    units = []
+    for _ in range(rng.randint(1, 6)):
+        n1 = rng.randint(1, 6)
+        causal_short = rng.random() < 0.5 and n1 > 1
+        units.append((n1 - 1 if causal_short else n1, n1))
+    bars = make_bars()
+    sim = Sim(rng, bars)
+    sim.run([(producer(bars, units, rng, skip), 'producer'),
+             (mma(bars, units, skip), 'mma'),
+             (softmax(bars, units, 0, rng, skip), 'softmax0'),
+             (softmax(bars, units, 1, rng, skip), 'softmax1')])
+    sim.check_races()
+    return units
+
+
+def test_pipeline_protocol_holds_under_random_timing():
+    for seed in range(400):
+        simulate(seed)
+
+
+@pytest.mark.parametrize("skip,where", [
+    # PV0 reading P0 before the softmax wrote it; the MMA thread then also
+    # runs two phases ahead of tile 0's S and O waits
+    (('p_full',), ('SP0', 'p_full0', 's_full0', 'o_full0')),
+    (('kv_empty',), ('K', 'V', 'kv_full')),      # K/V copied over slots still being read
+    (('release_early',), ('K', 'V', 'kv_full')),  # a group released before its readers ran
+    (('q_empty_early',), ('Q', 'q_full')),        # Q released before the last S MMA is issued
+])
+def test_planted_mistake_is_caught(skip, where):
+    caught = 0
+    for seed in range(400):
+        try:
+            simulate(seed, skip)
+        except Violation as e:
+            assert any(w in str(e) for w in where), str(e)
+            caught += 1
+    assert caught > 0

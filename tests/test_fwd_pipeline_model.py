@@ -1,4 +1,6 @@
-"""CPU model of the D = 128 forward kernel's pipeline protocol (no GPU).
+"""CPU models of the forward kernel's pipeline protocols (no GPU): D = 128
+(two ping-pong query tiles, grouped K/V ring) and D = 256 (one query tile, two
+S buffers, a ring of K/V half-slots).
 
 The forward runs, per CTA, a producer warp (the unit's two Q tiles, then K and
 V through a ring of four shared-memory slots used as two groups {V_j, K_j+1},
@@ -18,6 +20,12 @@ causal tile counts (tile 0 one key tile short), checking that every role
 finishes, that every parity wait sees exactly its phase, and that no buffer
 (Q, the K and V slots, S/P and O in TMEM) is written while a previous use is
 still read.  Planted mistakes (a wait or a release moved) must be caught.
+
+D = 256: S(j+1) goes into the other of two TMEM S buffers as soon as K_j+1's
+halves are in, before P(j) is waited for; K (head-dim halves) and V (key
+halves) stream through one ring of five half-slots in the order the MMAs read
+them, each released by a commit after its MMAs; a rescale of O waits for
+PV(j-1) on its own barrier, since the commit of S(j) no longer covers it.
 """
 import random
 
@@ -174,6 +182,148 @@ def test_planted_mistake_is_caught(skip, where):
     for seed in range(400):
         try:
             simulate(seed, skip)
+        except Violation as e:
+            assert any(w in str(e) for w in where), str(e)
+            caught += 1
+    assert caught > 0
+
+
+# ---------------------------------------------------------------- D = 256
+
+HALF_SLOTS = 5  # the ring of 32 KB half-slots: K head-dim halves, V key halves
+
+
+def make_bars_d256():
+    B = Barrier
+    bars = {'q_full': B('q_full', 1), 'q_empty': B('q_empty', 1),
+            'o_full': B('o_full', 1), 'pv_done': B('pv_done', 1)}
+    for i in range(HALF_SLOTS):
+        bars[f'hs_full{i}'] = B(f'hs_full{i}', 1)
+        bars[f'hs_empty{i}'] = B(f'hs_empty{i}', 1)
+    for buf in range(2):
+        bars[f's_full{buf}'] = B(f's_full{buf}', 1)
+        bars[f'p_full{buf}'] = B(f'p_full{buf}', 1)
+    return bars
+
+
+def producer_d256(b, units, rng, skip=()):
+    """Q, then K_0's halves, then per key tile j: K_j+1's halves (if any) and
+    V_j's halves: load r goes to half-slot r % 5."""
+    ring = [0]
+    f = rng.uniform(0.1, 5.0)
+
+    def load_half(what):  # what: 'K' or 'V' (the slot is the same either way)
+        hs, use = ring[0] % HALF_SLOTS, ring[0] // HALF_SLOTS
+        if 'hs_empty' not in skip:
+            yield ('wait', b[f'hs_empty{hs}'], (use & 1) ^ 1, use - 1)
+        yield ('arrive_tx', b[f'hs_full{hs}'], 1)
+        yield ('tma', b[f'hs_full{hs}'], 1, f'HS{hs}', use)
+        yield ('delay', f * rng.uniform(0, 30))
+        ring[0] += 1
+
+    for u, n in enumerate(units):
+        yield ('wait', b['q_empty'], (u & 1) ^ 1, u - 1)
+        yield ('arrive_tx', b['q_full'], 1)
+        yield ('tma', b['q_full'], 1, 'Q', u)
+        yield from load_half('K')
+        yield from load_half('K')
+        for j in range(n):
+            if j + 1 < n:
+                yield from load_half('K')
+                yield from load_half('K')
+            yield from load_half('V')
+            yield from load_half('V')
+
+
+def mma_d256(b, units, skip=()):
+    """S(j+1) into the other S buffer as soon as K_j+1 is in, then [P(j)] PV(j);
+    tile g (over the CTA's units) uses S buffer g & 1."""
+    kc = [0]
+    g = 0
+
+    def next_half():
+        hs, use = kc[0] % HALF_SLOTS, kc[0] // HALF_SLOTS
+        yield ('wait', b[f'hs_full{hs}'], use & 1, use)
+        kc[0] += 1
+        return (f'HS{hs}', use), hs
+
+    def issue_s(buf, gg, u):
+        for _ in range(2):
+            res, hs = yield from next_half()
+            yield ('mma', [('Q', u), res], [(f'SB{buf}', 2 * (gg >> 1))])
+            yield ('commit', b[f'hs_empty{hs}'])
+        yield ('commit', b[f's_full{buf}'])
+
+    for u, n in enumerate(units):
+        yield ('wait', b['q_full'], u & 1, u)
+        yield from issue_s(g & 1, g, u)
+        if n == 1:
+            yield ('commit', b['q_empty'])
+        for j in range(n):
+            if j + 1 < n:
+                yield from issue_s((g + 1) & 1, g + 1, u)
+                if j + 2 == n:
+                    yield ('commit', b['q_empty'])  # the last S MMA
+            yield ('wait', b[f'p_full{g & 1}'], (g >> 1) & 1, g >> 1)
+            for _ in range(2):
+                res, hs = yield from next_half()
+                yield ('mma', [(f'SB{g & 1}', 2 * (g >> 1) + 1), res], [('O', (u, 2 * j))])
+                yield ('commit', b[f'hs_empty{hs}'])
+            yield ('commit', b['pv_done'])
+            if j + 1 == n:
+                yield ('commit', b['o_full'])
+            g += 1
+
+
+def softmax_d256(b, units, rng, skip=()):
+    f = rng.uniform(0.1, 5.0)
+    g = 0
+    for u, n in enumerate(units):
+        for j in range(n):
+            buf = g & 1
+            yield ('wait', b[f's_full{buf}'], (g >> 1) & 1, g >> 1)
+            yield ('ld', f'SB{buf}', 2 * (g >> 1))
+            if j > 0 and rng.random() < 0.3:
+                # rescale: S(j) was issued before PV(j-1), so wait for that PV
+                if 'pv_done' not in skip:
+                    yield ('wait', b['pv_done'], (g - 1) & 1, g - 1)
+                yield ('ld', 'O', (u, 2 * j - 2))
+                yield ('st', 'O', (u, 2 * j - 1))
+            yield ('delay', f * rng.uniform(300, 1500))
+            yield ('st', f'SB{buf}', 2 * (g >> 1) + 1)
+            yield ('arrive', b[f'p_full{buf}'])
+            g += 1
+        yield ('wait', b['o_full'], u & 1, u)
+        yield ('ld', 'O', (u, 2 * (n - 1)))
+        yield ('delay', f * rng.uniform(200, 3000))  # direct stores, LSE
+
+
+def simulate_d256(seed, skip=()):
+    rng = random.Random(seed)
+    units = [rng.randint(1, 7) for _ in range(rng.randint(1, 6))]
+    bars = make_bars_d256()
+    sim = Sim(rng, bars)
+    sim.run([(producer_d256(bars, units, rng, skip), 'producer'),
+             (mma_d256(bars, units, skip), 'mma'),
+             (softmax_d256(bars, units, rng, skip), 'softmax')])
+    sim.check_races()
+    return units
+
+
+def test_d256_pipeline_protocol_holds_under_random_timing():
+    for seed in range(400):
+        simulate_d256(seed)
+
+
+@pytest.mark.parametrize("skip,where", [
+    (('pv_done',), ('O',)),             # rescale of O racing PV(j-1), issued after S(j)
+    (('hs_empty',), ('HS', 'hs_full')),  # a half-slot refilled while an MMA reads it
+])
+def test_d256_planted_mistake_is_caught(skip, where):
+    caught = 0
+    for seed in range(400):
+        try:
+            simulate_d256(seed, skip)
         except Violation as e:
             assert any(w in str(e) for w in where), str(e)
             caught += 1

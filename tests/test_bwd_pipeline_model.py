@@ -22,8 +22,13 @@ in a discrete-event simulation with random durations.  It checks that
 tcgen05 MMAs from the one issuing thread execute in issue order; a commit
 arrives once every MMA issued before it has completed.  Both producer orders
 are covered: the unit's K/V copy first (fixed-order instance) and after the
-first block's Q and dO copies (atomic order).  Planted mistakes (a wait left
-out) must be caught, which shows the checks can fail.
+first block's Q and dO copies (atomic order).  The D = 256 kernel (units of
+one output half, 64-query blocks, Q in two head-dim halves) has a model of its
+own below.  Planted mistakes (a wait left out, a release moved early) must be
+caught, which shows the checks can fail; two waits of the P/dS warps (for dS
+to have been read, and at D = 256 for the LSE/Delta rows) turned out to be
+implied by other orderings, so leaving them out is not a mistake the model
+can catch.
 """
 import random
 
@@ -219,5 +224,174 @@ def test_planted_missing_wait_is_caught(skip, where):
         except Violation as e:
             wheres = where if isinstance(where, tuple) else (where,)
             assert any(w in str(e) for w in wheres), str(e)
+            caught += 1
+    assert caught > 0
+
+
+# ---------------------------------------------------------------- D = 256
+#
+# A unit is (key tile, output half oh); queries stream in 64-row blocks.  Q
+# comes in two head-dim halves with their own barriers (dK of half oh reads
+# only Q half oh, so the other, "early" half is released once S^T is done and
+# the next block's copy of it loads while dP, dV and dK run); LSE and Delta
+# go through two shared-memory buffers by block parity.  The MMAs of a block
+# run in order S^T (early half first), dP^T, dV, dK, dQ^T; TMEM X holds S^T
+# then P^T, Y holds dP^T, then dS^T (written by the softmax warps), then dQ^T.
+
+
+def make_bars_d256():
+    B = Barrier
+    bars = {}
+    for name in ('kv_full', 'kv_empty', 'do_full', 'do_empty', 's_full', 'dp_full', 'p_ready',
+                 'ds_ready', 'dq_full', 'dq_empty', 'dkdv_full', 'dkdv_empty'):
+        bars[name] = B(name, 1)
+    for i in range(2):
+        bars[f'qh_full{i}'] = B(f'qh_full{i}', 1)
+        bars[f'qh_empty{i}'] = B(f'qh_empty{i}', 1)
+        bars[f'st_full{i}'] = B(f'st_full{i}', 1)
+    return bars
+
+
+def producer_d256(b, units, rng):
+    f = rng.uniform(0.1, 5.0)
+    n = 0
+    for u, (nb, oh) in enumerate(units):
+        yield ('wait', b['kv_empty'], (u & 1) ^ 1, u - 1)
+        yield ('arrive_tx', b['kv_full'], 2)
+        yield ('tma', b['kv_full'], 1, 'K', u)
+        yield ('tma', b['kv_full'], 1, 'V', u)
+        eh, lh = 1 - oh, oh
+        for _ in range(nb):
+            yield ('delay', f * rng.uniform(0, 50))  # LSE / Delta loads issued
+
+            def load_q_half(hs, n=n):
+                yield ('wait', b[f'qh_empty{hs}'], (n & 1) ^ 1, n - 1)
+                yield ('arrive_tx', b[f'qh_full{hs}'], 1)
+                yield ('tma', b[f'qh_full{hs}'], 1, f'Qh{hs}', n)
+            yield from load_q_half(eh)
+            yield ('delay', f * rng.uniform(0, 1500))  # the loads' latency
+            # buffer n & 1 was last read by the softmax of block n-2, whose dS
+            # preceded dQ^T(n-2) and so S^T(n-1), whose first half's release
+            # (or a later one) the early-half wait above has seen
+            yield ('st', f'ST{n & 1}', n >> 1)
+            yield ('arrive', b[f'st_full{n & 1}'])
+            yield ('wait', b['do_empty'], (n & 1) ^ 1, n - 1)
+            yield ('arrive_tx', b['do_full'], 1)
+            yield ('tma', b['do_full'], 1, 'dO', n)
+            yield from load_q_half(lh)
+            n += 1
+
+
+def mma_d256(b, units, skip=()):
+    n = 0
+    for u, (nb, oh) in enumerate(units):
+        yield ('wait', b['kv_full'], u & 1, u)
+        eh, lh = 1 - oh, oh
+        for i in range(nb):
+            for g2 in range(2):
+                hs = lh if g2 else eh
+                if g2 == 0 and 'qh_early' in skip:
+                    yield ('commit', b[f'qh_empty{eh}'])  # planted: before S^T reads it
+                yield ('wait', b[f'qh_full{hs}'], n & 1, n)
+                yield ('mma', [('K', u), (f'Qh{hs}', n)], [('X', 2 * n)])
+                if g2 == 0 and 'qh_early' not in skip:
+                    yield ('commit', b[f'qh_empty{eh}'])  # dK reads only half lh
+            yield ('commit', b['s_full'])
+            if n > 0 and 'dq_empty' not in skip:
+                yield ('wait', b['dq_empty'], (n - 1) & 1, n - 1)
+            yield ('wait', b['do_full'], n & 1, n)
+            yield ('mma', [('V', u), ('dO', n)], [('Y', 3 * n)])
+            yield ('commit', b['dp_full'])
+            yield ('wait', b['p_ready'], n & 1, n)
+            if i == 0 and u > 0 and 'dkdv_empty' not in skip:
+                yield ('wait', b['dkdv_empty'], (u - 1) & 1, u - 1)
+            yield ('mma', [('X', 2 * n + 1), ('dO', n)], [('dVacc', u)])
+            yield ('commit', b['do_empty'])
+            yield ('wait', b['ds_ready'], n & 1, n)
+            yield ('mma', [('Y', 3 * n + 1), (f'Qh{lh}', n)], [('dKacc', u)])
+            yield ('commit', b[f'qh_empty{lh}'])
+            yield ('mma', [('K', u), ('dS', n)], [('Y', 3 * n + 2)])
+            yield ('commit', b['dq_full'])
+            if i + 1 == nb:
+                yield ('commit', b['dkdv_full'])
+                yield ('commit', b['kv_empty'])
+            n += 1
+
+
+def softmax_d256(b, units, rng, skip=()):
+    f = rng.uniform(0.1, 5.0)
+    n = 0
+    for nb, _ in units:
+        for _ in range(nb):
+            # (also implied: the stats are written before the late Q half's
+            # copy, which S^T waits for)
+            yield ('wait', b[f'st_full{n & 1}'], (n >> 1) & 1, n >> 1)
+            yield ('wait', b['s_full'], n & 1, n)
+            yield ('ld', 'X', 2 * n)
+            yield ('ld', f'ST{n & 1}', n >> 1)
+            yield ('delay', f * rng.uniform(300, 1500))
+            yield ('st', 'X', 2 * n + 1)
+            yield ('arrive', b['p_ready'])
+            yield ('wait', b['dp_full'], n & 1, n)
+            if n > 0:
+                # the dQ MMA of the previous block has read dS (also implied by
+                # dp_full: dP^T(i) is issued after dQ^T(i-1))
+                yield ('wait', b['dq_full'], (n - 1) & 1, n - 1)
+            yield ('ld', 'Y', 3 * n)
+            yield ('ld', f'ST{n & 1}', n >> 1)
+            yield ('delay', f * rng.uniform(100, 800))
+            yield ('st', 'Y', 3 * n + 1)
+            yield ('st', 'dS', n)
+            yield ('arrive', b['ds_ready'])
+            n += 1
+
+
+def drain_d256(b, units, rng):
+    f = rng.uniform(0.1, 5.0)
+    n = 0
+    for u, (nb, _) in enumerate(units):
+        for _ in range(nb):
+            yield ('wait', b['dq_full'], n & 1, n)
+            yield ('ld', 'Y', 3 * n + 2)
+            yield ('arrive', b['dq_empty'])
+            yield ('delay', f * rng.uniform(200, 2000))  # staging and reductions
+            n += 1
+        yield ('wait', b['dkdv_full'], u & 1, u)
+        yield ('ld', 'dVacc', u)
+        yield ('ld', 'dKacc', u)
+        yield ('arrive', b['dkdv_empty'])
+        yield ('delay', f * rng.uniform(200, 3000))  # stores
+
+
+def simulate_d256(seed, skip=()):
+    rng = random.Random(seed)
+    units = [(rng.randint(1, 6), rng.randint(0, 1)) for _ in range(rng.randint(1, 8))]
+    bars = make_bars_d256()
+    sim = Sim(rng, bars)
+    sim.run([(producer_d256(bars, units, rng), 'producer'),
+             (mma_d256(bars, units, skip), 'mma'),
+             (softmax_d256(bars, units, rng, skip), 'softmax'),
+             (drain_d256(bars, units, rng), 'drain')])
+    sim.check_races()
+    return units
+
+
+def test_d256_pipeline_protocol_holds_under_random_timing():
+    for seed in range(400):
+        simulate_d256(seed)
+
+
+@pytest.mark.parametrize("skip,where", [
+    (('dq_empty',), ('Y', 'dq_full', 'dq_empty')),      # dP^T over dQ^T before the drain read it
+    (('qh_early',), ('Qh', 'qh_full')),                 # early Q half released before S^T read it
+    (('dkdv_empty',), ('dVacc', 'dKacc', 'dkdv_full')),  # next unit's dV over the unread accumulator
+])
+def test_d256_planted_missing_wait_is_caught(skip, where):
+    caught = 0
+    for seed in range(400):
+        try:
+            simulate_d256(seed, skip)
+        except Violation as e:
+            assert any(w in str(e) for w in where), str(e)
             caught += 1
     assert caught > 0

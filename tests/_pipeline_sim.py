@@ -38,10 +38,18 @@ class Sim:
                                    hardware test is done & 1 != parity
     ('arrive', bar) / ('arrive_tx', bar, n)
     ('tma', bar, n, res, use)      copy into res (use), n units of tx on landing
-    ('mma', reads, writes)         in-order tensor-pipe op, [(res, use)] lists
-    ('commit', bar)                arrive when every MMA issued so far is done
+    ('mma', reads, writes[, pipe]) in-order tensor-pipe op, [(res, use)] lists
+    ('commit', bar[, pipe])        arrive when every MMA issued so far to the
+                                   pipe (one per SM) is done
     ('ld', res, use) / ('st', res, use)   a thread access
     ('delay', t)
+    ('copy', bar, n, src, src_use, dst, dst_use, key)
+                                   a bulk copy between shared memories (also
+                                   to the other CTA of a pair): reads src and
+                                   writes dst until it lands, then n units of
+                                   tx complete on bar
+    ('wait_read', key)             until the last copy issued under key has
+                                   read its source (bulk wait_group.read)
     """
 
     def __init__(self, rng, bars):
@@ -54,9 +62,10 @@ class Sim:
         self.events = []
         self.seq = 0
         self.bars = bars
-        self.pipe_free = 0.0
+        self.pipe_free = {}  # tensor pipe (one per SM) -> when its last MMA ends
         self.acc = {}  # res -> list of (kind, use, start, end, who)
         self.blocked = {}
+        self.copy_done = {}  # key -> when the last copy under key has read its source
 
     def at(self, t, fn):
         self.seq += 1
@@ -121,10 +130,11 @@ class Sim:
                     self.complete_check(b)
                 self.at(land, landed)
             elif op == 'mma':
-                _, reads, writes = a
-                start = max(self.t, self.pipe_free)
+                reads, writes = a[1], a[2]
+                pipe = a[3] if len(a) > 3 else None
+                start = max(self.t, self.pipe_free.get(pipe, 0.0))
                 end = start + self.rng.uniform(200, 700) * self.mma_scale
-                self.pipe_free = end
+                self.pipe_free[pipe] = end
                 for res, use in reads:
                     self.record(res, 'r', use, start, end, who + ':mma')
                 for res, use in writes:
@@ -132,9 +142,26 @@ class Sim:
                 # issue returns when the pipe takes the MMA
                 self.at(max(self.t, start) + self.rng.uniform(5, 60), lambda p=proc: self.step(p))
                 return
+            elif op == 'copy':
+                _, b, n, src, src_use, dst, dst_use, key = a
+                land = self.t + self.rng.uniform(*self.tma_lat) * 0.5
+                self.record(src, 'r', src_use, self.t, land, who + ':copy')
+                self.record(dst, 'w', dst_use, self.t, land, who + ':copy')
+                self.copy_done[key] = land
+
+                def copied(b=b, n=n):
+                    b.tx -= n
+                    self.complete_check(b)
+                self.at(land, copied)
+            elif op == 'wait_read':
+                t_read = self.copy_done.get(a[1], self.t)
+                if t_read > self.t:
+                    self.at(t_read, lambda p=proc: self.step(p))
+                    return
             elif op == 'commit':
                 b = a[1]
-                self.at(max(self.t, self.pipe_free), lambda b=b: self.arrive(b))
+                pipe = a[2] if len(a) > 2 else None
+                self.at(max(self.t, self.pipe_free.get(pipe, 0.0)), lambda b=b: self.arrive(b))
             elif op in ('ld', 'st'):
                 _, res, use = a
                 d = self.rng.uniform(20, 200)

@@ -1,6 +1,7 @@
 """CPU models of the forward kernel's pipeline protocols (no GPU): D = 128
-(two ping-pong query tiles, grouped K/V ring) and D = 256 (one query tile, two
-S buffers, a ring of K/V half-slots).
+(two ping-pong query tiles, grouped K/V ring), D = 64 (the same tiles, K and V
+in single slots released by MMA commits) and D = 256 (one query tile, two S
+buffers, a ring of K/V half-slots).
 
 The forward runs, per CTA, a producer warp (the unit's two Q tiles, then K and
 V through a ring of four shared-memory slots used as two groups {V_j, K_j+1},
@@ -114,7 +115,7 @@ def mma(b, units, skip=()):
                 yield ('commit', b['o_full1'])
 
 
-def softmax(b, units, t, rng, skip=()):
+def softmax(b, units, t, rng, skip=(), grouped=True):
     f = rng.uniform(0.1, 5.0)
     jj = 0
     grp = 0  # groups released (tile 1)
@@ -122,7 +123,7 @@ def softmax(b, units, t, rng, skip=()):
         n = n1 if t else n0
         for j in range(n):
             yield ('wait', b[f's_full{t}'], jj & 1, jj)
-            if t == 1:
+            if t == 1 and grouped:
                 yield ('arrive', b[f'kv_empty{grp % GROUPS}'])
                 grp += 1
                 if 'release_early' in skip and j == 0:
@@ -140,7 +141,7 @@ def softmax(b, units, t, rng, skip=()):
             yield ('arrive', b[f'p_full{t}'])
             jj += 1
         yield ('wait', b[f'o_full{t}'], u & 1, u)
-        if t == 1 and 'release_early' not in skip:
+        if t == 1 and grouped and 'release_early' not in skip:
             yield ('arrive', b[f'kv_empty{grp % GROUPS}'])  # the unit's last group
             grp += 1
         yield ('ld', f'O{t}', (u, 2 * (n - 1)))
@@ -184,6 +185,132 @@ def test_planted_mistake_is_caught(skip, where):
             simulate(seed, skip)
         except Violation as e:
             assert any(w in str(e) for w in where), str(e)
+            caught += 1
+    assert caught > 0
+
+
+# ---------------------------------------------------------------- D = 64
+#
+# Single slots: K_j and V_j each in a slot of an eight-slot ring with its own
+# full and empty barriers, released by MMA commits (K_j after S1(j), V_j
+# after PV1(j)); the softmax warps release nothing.
+
+STAGES = 8
+
+
+def make_bars_d64():
+    B = Barrier
+    bars = {'q_full': B('q_full', 1), 'q_empty': B('q_empty', 1)}
+    for i in range(STAGES):
+        bars[f'kv_full{i}'] = B(f'kv_full{i}', 1)
+        bars[f'kv_empty{i}'] = B(f'kv_empty{i}', 1)
+    for t in range(2):
+        bars[f's_full{t}'] = B(f's_full{t}', 1)
+        bars[f'p_full{t}'] = B(f'p_full{t}', 1)
+        bars[f'o_full{t}'] = B(f'o_full{t}', 1)
+    return bars
+
+
+def producer_d64(b, units, rng):
+    ring = 0
+    f = rng.uniform(0.1, 5.0)
+    for u, (n0, n1) in enumerate(units):
+        yield ('wait', b['q_empty'], (u & 1) ^ 1, u - 1)
+        yield ('arrive_tx', b['q_full'], 1)
+        yield ('tma', b['q_full'], 1, 'Q', u)
+        for j in range(n1):
+            for _ in ('K', 'V'):
+                sl, use = ring % STAGES, ring // STAGES
+                yield ('wait', b[f'kv_empty{sl}'], (use & 1) ^ 1, use - 1)
+                yield ('arrive_tx', b[f'kv_full{sl}'], 1)
+                yield ('tma', b[f'kv_full{sl}'], 1, f'slot{sl}', use)
+                yield ('delay', f * rng.uniform(0, 30))
+                ring += 1
+
+
+def mma_d64(b, units, skip=()):
+    ring = 0
+    jj = [0, 0]
+    for u, (n0, n1) in enumerate(units):
+        yield ('wait', b['q_full'], u & 1, u)
+        ks, kuse = ring % STAGES, ring // STAGES
+        yield ('wait', b[f'kv_full{ks}'], kuse & 1, kuse)
+        ring += 1
+        yield ('mma', [('Q', u), (f'slot{ks}', kuse)], [('SP0', 2 * jj[0])])
+        yield ('commit', b['s_full0'])
+        yield ('mma', [('Q', u), (f'slot{ks}', kuse)], [('SP1', 2 * jj[1])])
+        yield ('commit', b['s_full1'])
+        yield ('commit', b[f'kv_empty{ks}'])
+        if n1 == 1:
+            yield ('commit', b['q_empty'])
+        for j in range(n1):
+            vs, vuse = ring % STAGES, ring // STAGES
+            yield ('wait', b[f'kv_full{vs}'], vuse & 1, vuse)
+            ring += 1
+            has_next = j + 1 < n1
+            if has_next:
+                ns, nuse = ring % STAGES, ring // STAGES
+                ring += 1
+            next_ready = False
+            if j < n0:
+                yield ('wait', b['p_full0'], jj[0] & 1, jj[0])
+                yield ('mma', [('SP0', 2 * jj[0] + 1), (f'slot{vs}', vuse)], [('O0', (u, 2 * j))])
+                jj[0] += 1
+                if j + 1 < n0:
+                    yield ('wait', b[f'kv_full{ns}'], nuse & 1, nuse)
+                    next_ready = True
+                    yield ('mma', [('Q', u), (f'slot{ns}', nuse)], [('SP0', 2 * jj[0])])
+                    yield ('commit', b['s_full0'])
+                else:
+                    yield ('commit', b['o_full0'])
+            if 'v_release_early' in skip:
+                yield ('commit', b[f'kv_empty{vs}'])  # planted: before PV1(j) reads V_j
+            yield ('wait', b['p_full1'], jj[1] & 1, jj[1])
+            yield ('mma', [('SP1', 2 * jj[1] + 1), (f'slot{vs}', vuse)], [('O1', (u, 2 * j))])
+            jj[1] += 1
+            if 'v_release_early' not in skip:
+                yield ('commit', b[f'kv_empty{vs}'])
+            if has_next:
+                if not next_ready:
+                    yield ('wait', b[f'kv_full{ns}'], nuse & 1, nuse)
+                yield ('mma', [('Q', u), (f'slot{ns}', nuse)], [('SP1', 2 * jj[1])])
+                yield ('commit', b['s_full1'])
+                yield ('commit', b[f'kv_empty{ns}'])
+                if j + 2 == n1:
+                    yield ('commit', b['q_empty'])
+            else:
+                yield ('commit', b['o_full1'])
+
+
+def simulate_d64(seed, skip=()):
+    rng = random.Random(seed)
+    units = []
+    for _ in range(rng.randint(1, 6)):
+        n1 = rng.randint(1, 7)
+        units.append((n1 - 1 if (rng.random() < 0.5 and n1 > 1) else n1, n1))
+    bars = make_bars_d64()
+    sim = Sim(rng, bars)
+    sim.run([(producer_d64(bars, units, rng), 'producer'),
+             (mma_d64(bars, units, skip), 'mma'),
+             (softmax(bars, units, 0, rng, skip, grouped=False), 'softmax0'),
+             (softmax(bars, units, 1, rng, skip, grouped=False), 'softmax1')])
+    sim.check_races()
+    return units
+
+
+def test_d64_pipeline_protocol_holds_under_random_timing():
+    for seed in range(400):
+        simulate_d64(seed)
+
+
+def test_d64_planted_mistake_is_caught():
+    # V_j's slot released before PV1(j) has read it
+    caught = 0
+    for seed in range(400):
+        try:
+            simulate_d64(seed, ('v_release_early',))
+        except Violation as e:
+            assert 'slot' in str(e) or 'kv_full' in str(e), str(e)
             caught += 1
     assert caught > 0
 

@@ -12,7 +12,10 @@ check, for many shapes, the properties the kernels rely on:
     groups of half a grid of heads when many heads' tensors exceed L2, and
     within each group every unit is at least as long as the next one;
   * the grouping condition itself (more heads than half the grid, their
-    tensors above the L2 size) switches on where it should.
+    tensors above the L2 size) switches on where it should;
+  * the D = 256 backward's and both CTA-pair kernels' unit maps are
+    bijections too, the D = 128 pairs cover every key tile once, and the
+    serpentine rounds hand every unit to exactly one CTA.
 """
 import itertools
 
@@ -125,3 +128,56 @@ def test_grouping_switches_on_only_for_many_heads_beyond_l2():
     assert fwd_group_size(256, G, 1024, 64) == 256
     assert fwd_group_size(256, G, 1024, 128) == 256
     assert bwd_group_size(256, G, 1024, 64) == 0
+
+
+def d256_unit(u, nT):
+    """(bh, key tile j, output half oh) of D = 256 backward unit u: the two
+    halves of a key tile, then the key tiles of a head, are adjacent."""
+    return (u >> 1) // nT, (u >> 1) % nT, u & 1
+
+
+def pair_unit(u, nP):
+    """(bh, key-tile pair p) of D = 128 CTA-pair unit u: a head's pairs in a row."""
+    return u // nP, u % nP
+
+
+def split_unit(u, BH, nT, causal):
+    """(bh, key tile j) of D = 256 split-pair unit u: tile-major under a causal
+    mask (longest first across heads), head by head otherwise."""
+    return (u % BH, u // BH) if causal else (u // nT, u % nT)
+
+
+@pytest.mark.parametrize("B,H,S", SHAPES)
+def test_other_backward_unit_maps_are_bijections(B, H, S):
+    BH = B * H
+    nT = (S + 127) // 128
+    seen = [d256_unit(u, nT) for u in range(BH * nT * 2)]
+    assert sorted(seen) == [(bh, j, oh) for bh in range(BH) for j in range(nT) for oh in range(2)]
+    nP = (nT + 1) // 2
+    seen = [pair_unit(u, nP) for u in range(BH * nP)]
+    assert sorted(seen) == [(bh, p) for bh in range(BH) for p in range(nP)]
+    # each pair covers key tiles 2p and 2p + 1 (the second past the end when
+    # nT is odd, which that CTA skips): every key tile exactly once
+    tiles = sorted((bh, 2 * p + r) for bh, p in seen for r in range(2) if 2 * p + r < nT)
+    assert tiles == [(bh, j) for bh in range(BH) for j in range(nT)]
+    for causal in (False, True):
+        seen = [split_unit(u, BH, nT, causal) for u in range(BH * nT)]
+        assert sorted(seen) == [(bh, j) for bh in range(BH) for j in range(nT)]
+        if causal:  # tile j has the most query blocks for j = 0: ascending j
+            assert [j for _, j in seen] == sorted(j for _, j in seen)
+
+
+@pytest.mark.parametrize("G", [1, 2, 7, 76, 152])
+@pytest.mark.parametrize("U", [1, 5, 151, 152, 153, 1000])
+def test_serpentine_rounds_cover_every_unit_once(G, U):
+    # CTA (or pair) c takes unit r * G + c in even rounds and r * G + G - 1 - c
+    # in odd rounds, while r * G < U
+    got = []
+    for c in range(G):
+        r = 0
+        while r * G < U:
+            u = r * G + (G - 1 - c if r & 1 else c)
+            if u < U:
+                got.append(u)
+            r += 1
+    assert sorted(got) == list(range(U))

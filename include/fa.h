@@ -232,8 +232,11 @@ fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *
  * Backward for callers that cannot allocate device memory: code that runs
  * where cudaMalloc is not allowed or not wanted (host callbacks, plug-ins
  * that only get their inputs and outputs from a host framework, tools that
- * must keep the device footprint fixed).  The pages have no counterpart of
- * this entry point; it exists for those callers only.
+ * must keep the device footprint fixed).  It computes what fa_bwd computes
+ * (the backward of "FlashAttention-4: Algorithm and Kernel Pipelining
+ * Co-Design for Asymmetric Hardware Scaling" (gist.science/nl), Technische
+ * samenvatting, Methodologie §3); the pages have no counterpart of this
+ * calling convention, which exists for those callers only.
  * Same arguments, results and errors as fa_bwd minus dq_acc and delta
  * (sizes that fa_bwd_workspace_size rejects give FA_ERR_INVALID_ARG); the
  * scratch comes from one fixed array of 72 MiB inside the library, held on
@@ -242,10 +245,10 @@ fa_status fa_bwd_varlen_deterministic(const void *q, const void *k, const void *
  * FA_ERR_INVALID_ARG.  The first call on each device, and the first call
  * after that device's context was replaced (cudaDeviceReset), looks up the
  * array's device address (make those calls before any stream capture).  All
- * calls on a
- * device share the array: calls whose kernels may overlap on the GPU race
- * and must be serialised by the caller.  Each call re-zeroes the part of the
- * scratch it uses, so nothing carries over between calls.  Allocates nothing.
+ * calls on a device share the array: calls whose kernels may overlap on the
+ * GPU race and must be serialised by the caller.  Each call re-zeroes the
+ * part of the scratch it uses, so nothing carries over between calls.
+ * Allocates nothing.
  */
 fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                          const void *dout, const float *lse, void *dq, void *dk, void *dv,
